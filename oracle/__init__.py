@@ -1,0 +1,214 @@
+"""Plain fp64 CPU oracle for the Packed Twin Inference hot path.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()`` and
+the CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product path (``stream_quantized_gemv_gb300``) never imports it, and this
+package never imports the product path: the two share no code.
+
+The arithmetic lives in ``pti_oracle.c`` (plain C99, double precision); this
+module compiles it with gcc and wraps it with ctypes, converting numpy arrays
+to pointers.  Every function cites the passage it follows in the C source.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_SOURCES = [os.path.join(_HERE, "pti_oracle.c")]
+_HEADERS = [os.path.join(_HERE, "pti_oracle.h")]
+
+_lib = None
+_lock = threading.Lock()
+
+Q8_BLOCK_BYTES = 34
+TWIN_BLOCK_BYTES = 68
+BLOCK_COLS = 32
+
+
+def _stale() -> bool:
+    if not os.path.exists(_LIB_PATH):
+        return True
+    built = os.path.getmtime(_LIB_PATH)
+    return any(os.path.getmtime(p) > built for p in _SOURCES + _HEADERS)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (plain gcc, -O2)."""
+    if force or _stale():
+        os.makedirs(_BUILD_DIR, exist_ok=True)
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-Wall", "-Wextra",
+               "-o", tmp] + _SOURCES + ["-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            I64 = ctypes.c_int64
+            I = ctypes.c_int
+            lib.pti_or_f16_to_f64.restype = ctypes.c_double
+            lib.pti_or_f16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.pti_or_q8_weight.restype = ctypes.c_double
+            lib.pti_or_q8_weight.argtypes = [P, I64, I64, I64]
+            lib.pti_or_twin_weight.restype = None
+            lib.pti_or_twin_weight.argtypes = [P, I64, I64, I64, P, P]
+            lib.pti_or_twin_pack.restype = I
+            lib.pti_or_twin_pack.argtypes = [P, P, I64, P]
+            lib.pti_or_twin_unpack.restype = I
+            lib.pti_or_twin_unpack.argtypes = [P, I64, P, P]
+            lib.pti_or_q8_gemv_rows.restype = I
+            lib.pti_or_q8_gemv_rows.argtypes = [P, I64, I64, I, P, P, I64, P, P]
+            lib.pti_or_twin_gemv_rows.restype = I
+            lib.pti_or_twin_gemv_rows.argtypes = [P, I64, I64, P, P, P, I64, P, P, P, P]
+            lib.pti_or_verify_greedy.restype = I
+            lib.pti_or_verify_greedy.argtypes = [P, P, I64, I, I64, P, P, P]
+            lib.pti_or_mlp_layer.restype = I
+            lib.pti_or_mlp_layer.argtypes = [P, P, P, I64, I64, I, ctypes.c_double, P, P, P]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    if not a.flags["C_CONTIGUOUS"]:
+        raise ValueError("oracle arrays must be C-contiguous")
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise ValueError(f"oracle {what}: bad argument")
+
+
+def f16_to_f64(h: int) -> float:
+    """Decode one IEEE-754 binary16 bit pattern exactly."""
+    return _load().pti_or_f16_to_f64(int(h) & 0xFFFF)
+
+
+def q8_weight(w: np.ndarray, cols: int, row: int, col: int) -> float:
+    return _load().pti_or_q8_weight(_ptr(w), cols, row, col)
+
+
+def twin_weight(w: np.ndarray, cols: int, row: int, col: int) -> tuple[float, float]:
+    a = ctypes.c_double()
+    b = ctypes.c_double()
+    _load().pti_or_twin_weight(_ptr(w), cols, row, col, ctypes.byref(a), ctypes.byref(b))
+    return a.value, b.value
+
+
+def twin_pack(qa: np.ndarray, qb: np.ndarray) -> np.ndarray:
+    """Two Q8 block streams (uint8, 34 bytes per block) -> one twin stream."""
+    qa = np.ascontiguousarray(qa, dtype=np.uint8).reshape(-1)
+    qb = np.ascontiguousarray(qb, dtype=np.uint8).reshape(-1)
+    if qa.size != qb.size or qa.size % Q8_BLOCK_BYTES:
+        raise ValueError("twin_pack: mismatched or partial blocks")
+    n_blocks = qa.size // Q8_BLOCK_BYTES
+    out = np.empty(n_blocks * TWIN_BLOCK_BYTES, dtype=np.uint8)
+    _check(_load().pti_or_twin_pack(_ptr(qa), _ptr(qb), n_blocks, _ptr(out)), "twin_pack")
+    return out
+
+
+def twin_unpack(twin: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    twin = np.ascontiguousarray(twin, dtype=np.uint8).reshape(-1)
+    if twin.size % TWIN_BLOCK_BYTES:
+        raise ValueError("twin_unpack: partial block")
+    n_blocks = twin.size // TWIN_BLOCK_BYTES
+    qa = np.empty(n_blocks * Q8_BLOCK_BYTES, dtype=np.uint8)
+    qb = np.empty(n_blocks * Q8_BLOCK_BYTES, dtype=np.uint8)
+    _check(_load().pti_or_twin_unpack(_ptr(twin), n_blocks, _ptr(qa), _ptr(qb)), "twin_unpack")
+    return qa, qb
+
+
+def q8_gemv(w: np.ndarray, rows: int, cols: int, x: np.ndarray, rows_idx=None):
+    """fp64 N-stream Q8 GEMV.  ``x`` is [n][cols] float32.
+
+    Returns ``(y, bound)``, both float64 [n][len(rows_idx)].
+    """
+    w = np.ascontiguousarray(w, dtype=np.uint8).reshape(-1)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if x.ndim == 1:
+        x = x[None, :]
+    n = x.shape[0]
+    if x.shape[1] != cols:
+        raise ValueError("q8_gemv: x has the wrong length")
+    if w.size != rows * (cols // BLOCK_COLS) * Q8_BLOCK_BYTES:
+        raise ValueError("q8_gemv: weight buffer has the wrong size")
+    idx = (np.arange(rows, dtype=np.int64) if rows_idx is None
+           else np.ascontiguousarray(rows_idx, dtype=np.int64))
+    y = np.empty((n, idx.size), dtype=np.float64)
+    bound = np.empty((n, idx.size), dtype=np.float64)
+    _check(_load().pti_or_q8_gemv_rows(_ptr(w), rows, cols, n, _ptr(x), _ptr(idx), idx.size,
+                                       _ptr(y), _ptr(bound)), "q8_gemv")
+    return y, bound
+
+
+def twin_gemv(w: np.ndarray, rows: int, cols: int, xa: np.ndarray, xb: np.ndarray, rows_idx=None):
+    """fp64 twin GEMV.  Returns ``(ya, yb, bound_a, bound_b)``."""
+    w = np.ascontiguousarray(w, dtype=np.uint8).reshape(-1)
+    xa = np.ascontiguousarray(xa, dtype=np.float32).reshape(-1)
+    xb = np.ascontiguousarray(xb, dtype=np.float32).reshape(-1)
+    if xa.size != cols or xb.size != cols:
+        raise ValueError("twin_gemv: x has the wrong length")
+    if w.size != rows * (cols // BLOCK_COLS) * TWIN_BLOCK_BYTES:
+        raise ValueError("twin_gemv: weight buffer has the wrong size")
+    idx = (np.arange(rows, dtype=np.int64) if rows_idx is None
+           else np.ascontiguousarray(rows_idx, dtype=np.int64))
+    out = [np.empty(idx.size, dtype=np.float64) for _ in range(4)]
+    _check(_load().pti_or_twin_gemv_rows(_ptr(w), rows, cols, _ptr(xa), _ptr(xb), _ptr(idx), idx.size,
+                                         *[_ptr(o) for o in out]), "twin_gemv")
+    return tuple(out)
+
+
+def verify_greedy(logits: np.ndarray, guess: np.ndarray):
+    """Greedy verify.  ``logits`` [steps][n][vocab] float32, ``guess`` [steps][n] int32.
+
+    Returns ``(argmax [steps][n] int32, match [steps][n-1] uint8, accept [steps] int32)``.
+    """
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    guess = np.ascontiguousarray(guess, dtype=np.int32)
+    steps, n, vocab = logits.shape
+    if guess.shape != (steps, n):
+        raise ValueError("verify_greedy: guess has the wrong shape")
+    argmax = np.empty((steps, n), dtype=np.int32)
+    match = np.empty((steps, max(n - 1, 0)), dtype=np.uint8)
+    accept = np.empty(steps, dtype=np.int32)
+    match_ptr = _ptr(match) if n > 1 else None
+    _check(_load().pti_or_verify_greedy(_ptr(logits), _ptr(guess), steps, n, vocab,
+                                        _ptr(argmax), match_ptr, _ptr(accept)), "verify_greedy")
+    return argmax, match, accept
+
+
+def mlp_layer(wg, wu, wd, hidden: int, ffn: int, x: np.ndarray, eps: float = 1e-6):
+    """One fp64 layer of the decode weight pass.  ``x`` [n][hidden] (any float dtype).
+
+    Returns ``(x_out [n][hidden] float64, h [n][ffn] float64 normalised)``.
+    """
+    wg = np.ascontiguousarray(wg, dtype=np.uint8).reshape(-1)
+    wu = np.ascontiguousarray(wu, dtype=np.uint8).reshape(-1)
+    wd = np.ascontiguousarray(wd, dtype=np.uint8).reshape(-1)
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    if x.ndim == 1:
+        x = x[None, :]
+    n = x.shape[0]
+    if wg.size != ffn * (hidden // BLOCK_COLS) * Q8_BLOCK_BYTES or wu.size != wg.size:
+        raise ValueError("mlp_layer: gate/up buffers have the wrong size")
+    if wd.size != hidden * (ffn // BLOCK_COLS) * Q8_BLOCK_BYTES:
+        raise ValueError("mlp_layer: down buffer has the wrong size")
+    x_out = np.empty((n, hidden), dtype=np.float64)
+    h = np.empty((n, ffn), dtype=np.float64)
+    _check(_load().pti_or_mlp_layer(_ptr(wg), _ptr(wu), _ptr(wd), hidden, ffn, n, eps,
+                                    _ptr(x), _ptr(x_out), _ptr(h)), "mlp_layer")
+    return x_out, h
