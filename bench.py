@@ -1,0 +1,512 @@
+"""Benchmark of the Packed Twin Inference hot path on GB300.
+
+Default line (N=1 GPU): the multi-stream Q8 weight pass, N = 4 activation
+streams through Qwen3.6-27B-shaped Q8 matrices (FFN 17408 x hidden 5120), one
+step = one pass over L distinct matrices (each weight read once per step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Metric: effective weight GB/s (algorithmic bytes / device time) with the
+fraction of the measured HBM copy bandwidth, plus stream-tokens/s per weight
+pass.  ``--impl reference`` times the fp64 CPU oracle on a bounded sample of
+the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import contextlib
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective weight GB/s (% of GB300 HBM peak) and stream-tokens/s per weight pass"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "stream_quantized_gemv_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("kernel_source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        # address the GPU by UUID: CUDA_VISIBLE_DEVICES may renumber devices
+        self.gpu_id = str(device_index)
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.gpu_id = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            pass
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.text = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.text, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = [r for r in csv.reader(io.StringIO(getattr(self, "text", ""))) if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(n_gpus: int):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+Q8_BLOCK = 34
+TWIN_BLOCK = 68
+
+
+class Q8Pass:
+    """N-stream Q8 GEMV over L distinct rows x cols matrices (one step = one pass)."""
+
+    def __init__(self, rows=17408, cols=5120, n=4, layers=16, seed=0):
+        import torch
+        import pti_synth
+        import stream_quantized_gemv_gb300 as pti
+        self.pti, self.torch = pti, torch
+        self.rows, self.cols, self.n, self.layers = rows, cols, n, layers
+        self.name = f"q8_gemv_n{n}_{rows}x{cols}_x{layers}"
+        self.w = [pti_synth.q8_matrix_device(rows, cols, seed, 1000 + i) for i in range(layers)]
+        self.x = pti_synth.activations_device(n, cols, seed, 1)
+        self.y = torch.empty((n, rows), dtype=torch.float32, device="cuda")
+        need = pti.q8_gemv_workspace_bytes(rows, cols, n)
+        self.ws = torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda")
+        self.weight_bytes = rows * (cols // 32) * Q8_BLOCK
+        self.launch_bytes = self.weight_bytes + 4 * n * (rows + cols)
+        self.step_bytes = layers * self.launch_bytes
+        self.launches_per_step = layers
+        self.tokens_per_step = n
+        self.dominant = "gemv_tma_kernel<Q8,%d>" % n
+        self.dtype = "f32 (int8 weights with binary16 block scales, exact dequantisation)"
+
+    def step(self, x=None, y=None):
+        x = self.x if x is None else x
+        y = self.y if y is None else y
+        for w in self.w:
+            self.pti.q8_gemv_nstream(w, self.rows, self.cols, x, y=y, ws=self.ws)
+
+    def e2e_buffers(self):
+        t = self.torch
+        hx = t.empty_like(self.x, device="cpu").pin_memory()
+        hx.copy_(self.x.cpu())
+        hy = t.empty_like(self.y, device="cpu").pin_memory()
+        return hx, hy, self.x, self.y
+
+    def config(self):
+        return {"workload": f"N-stream Q8 GEMV weight pass: {self.layers} distinct {self.rows}x{self.cols} "
+                            f"Q8 matrices (f16 scale + 32 int8 per 34-byte block), N={self.n} fp32 streams",
+                "rows": self.rows, "cols": self.cols, "n_streams": self.n, "matrices_per_step": self.layers,
+                "weight_bytes_per_step": self.layers * self.weight_bytes,
+                "l2": f"inputs larger than L2: {self.layers * self.weight_bytes / 1e9:.2f} GB of distinct "
+                      "weights per step, streamed with an L2 evict-first policy"}
+
+    def cpu_sample(self):
+        import oracle
+        import pti_synth
+        rows = 48
+        w = pti_synth.q8_matrix(rows, self.cols, seed=0, tensor_id=1)
+        x = pti_synth.activations(self.n, self.cols, seed=0, tensor_id=1)
+        sample_bytes = rows * (self.cols // 32) * Q8_BLOCK + 4 * self.n * (rows + self.cols)
+
+        def run():
+            oracle.q8_gemv(w, rows, self.cols, x)
+        return run, sample_bytes, f"oracle q8_gemv on {rows} of the {self.rows} rows, N={self.n}"
+
+
+class TwinPass(Q8Pass):
+    def __init__(self, rows=17408, cols=5120, layers=8, seed=0):
+        import torch
+        import pti_synth
+        import stream_quantized_gemv_gb300 as pti
+        self.pti, self.torch = pti, torch
+        self.rows, self.cols, self.n, self.layers = rows, cols, 2, layers
+        self.name = f"ssq_twin_gemv_{rows}x{cols}_x{layers}"
+        self.w = [pti_synth.twin_matrix_device(rows, cols, seed, 2000 + i) for i in range(layers)]
+        self.x = pti_synth.activations_device(2, cols, seed, 2)
+        self.y = torch.empty((2, rows), dtype=torch.float32, device="cuda")
+        need = pti.ssq_twin_gemv_workspace_bytes(rows, cols)
+        self.ws = torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda")
+        self.weight_bytes = rows * (cols // 32) * TWIN_BLOCK
+        self.launch_bytes = self.weight_bytes + 4 * 2 * (rows + cols)
+        self.step_bytes = layers * self.launch_bytes
+        self.launches_per_step = layers
+        self.tokens_per_step = 2
+        self.dominant = "gemv_tma_kernel<Twin>"
+        self.dtype = "f32 (two int8 models packed per uint16, binary16 scales, exact dequantisation)"
+
+    def step(self, x=None, y=None):
+        x = self.x if x is None else x
+        y = self.y if y is None else y
+        for w in self.w:
+            self.pti.ssq_twin_gemv(w, self.rows, self.cols, x[0], x[1], y_a=y[0], y_b=y[1], ws=self.ws)
+
+    def config(self):
+        return {"workload": f"SSQ mode-16 twin GEMV: {self.layers} distinct {self.rows}x{self.cols} twin "
+                            "matrices (68-byte blocks), streams A and B",
+                "rows": self.rows, "cols": self.cols, "matrices_per_step": self.layers,
+                "weight_bytes_per_step": self.layers * self.weight_bytes,
+                "l2": f"inputs larger than L2: {self.layers * self.weight_bytes / 1e9:.2f} GB per step"}
+
+    def cpu_sample(self):
+        import oracle
+        import pti_synth
+        rows = 48
+        w = pti_synth.twin_matrix(rows, self.cols, seed=0, tensor_id=1)
+        xa, xb = pti_synth.activations(2, self.cols, seed=0, tensor_id=2)
+        sample_bytes = rows * (self.cols // 32) * TWIN_BLOCK + 8 * (rows + self.cols)
+
+        def run():
+            oracle.twin_gemv(w, rows, self.cols, xa, xb)
+        return run, sample_bytes, f"oracle twin_gemv on {rows} of the {self.rows} rows"
+
+
+class VerifyBatch(Q8Pass):
+    def __init__(self, steps=4096, n=4, vocab=151936, p=0.6, seed=0):
+        import torch
+        import pti_synth
+        import stream_quantized_gemv_gb300 as pti
+        self.pti, self.torch = pti, torch
+        self.steps, self.n, self.vocab, self.p = steps, n, vocab, p
+        self.name = f"verify_greedy_{steps}x{n}x{vocab}"
+        self.logits, self.guess, _ = pti_synth.verify_batch_device(steps, n, vocab, p, seed)
+        self.out = (torch.empty((steps, n), dtype=torch.int32, device="cuda"),
+                    torch.empty((steps, n - 1), dtype=torch.uint8, device="cuda"),
+                    torch.empty(steps, dtype=torch.int32, device="cuda"))
+        self.launch_bytes = steps * n * vocab * 4 + steps * n * 4 * 2 + steps * (n - 1) + steps * 4
+        self.step_bytes = self.launch_bytes
+        self.launches_per_step = 1
+        self.tokens_per_step = steps * n
+        self.dominant = "verify_greedy_kernel"
+        self.dtype = "f32 compare, int32 indices"
+        self.x = self.logits
+        self.y = self.out[2]
+
+    def step(self, x=None, y=None):
+        self.pti.verify_greedy(self.logits, self.guess, *self.out)
+
+    def config(self):
+        return {"workload": f"greedy verify batch {self.steps} steps x {self.n} streams x vocab {self.vocab}, "
+                            f"N(0,3) logits, planted guesses p={self.p}",
+                "l2": f"inputs larger than L2: {self.launch_bytes / 1e9:.2f} GB of logits per step"}
+
+    def cpu_sample(self):
+        import oracle
+        import pti_synth
+        steps = 24
+        lg, gs, _ = pti_synth.verify_batch(steps, self.n, self.vocab, self.p, seed=0)
+        b = steps * self.n * self.vocab * 4
+
+        def run():
+            oracle.verify_greedy(lg, gs)
+        return run, b, f"oracle verify_greedy on {steps} of the {self.steps} steps"
+
+
+WORKLOADS = {
+    "q8": lambda a: Q8Pass(a.rows or 17408, a.cols or 5120, a.n, a.layers or 16),
+    "twin": lambda a: TwinPass(a.rows or 17408, a.cols or 5120, a.layers or 8),
+    "verify": lambda a: VerifyBatch(),
+}
+
+
+# ---------------------------------------------------------------------------
+# timing
+# ---------------------------------------------------------------------------
+def time_gpu(wl, steps, warmup, world, local):
+    import torch
+    torch.cuda.synchronize()
+    for _ in range(warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    # CUDA graph of one step (all launches of the pass), replayed K times
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        wl.step()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            wl.step()
+    torch.cuda.synchronize()
+    for _ in range(max(1, warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ms, world)
+    return ms / steps, clk.summary()
+
+
+def time_e2e(wl, steps, warmup):
+    """Same pass through the public API with inputs in pinned host memory:
+    per step H2D of the activations, the pass, D2H of the result."""
+    import torch
+    if isinstance(wl, VerifyBatch):
+        hx = torch.empty_like(wl.guess, device="cpu").pin_memory()
+        hx.copy_(wl.guess.cpu())
+        dx = wl.guess
+        hy = torch.empty_like(wl.out[2], device="cpu").pin_memory()
+        dy = wl.out[2]
+    else:
+        hx, hy, dx, dy = wl.e2e_buffers()
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        dx.copy_(hx, non_blocking=True)
+        wl.step()
+        hy.copy_(dy, non_blocking=True)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        dx.copy_(hx, non_blocking=True)
+        wl.step()
+        hy.copy_(dy, non_blocking=True)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    return ms, hx.numel() * hx.element_size(), hy.numel() * hy.element_size()
+
+
+def time_cpu(wl, budget_s=12.0):
+    run, sample_bytes, what = wl.cpu_sample()
+    t0 = time.perf_counter()
+    run()
+    one = time.perf_counter() - t0
+    reps = max(1, min(100000, int(budget_s / max(one, 1e-6))))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        run()
+    dt = (time.perf_counter() - t0) / reps
+    return sample_bytes / dt / 1e9, what, dt
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="q8", choices=sorted(WORKLOADS) + ["all"])
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--n", type=int, default=4)
+    ap.add_argument("--rows", type=int, default=0)
+    ap.add_argument("--cols", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    a.warmup = max(a.warmup, 3)
+
+    rank, world, local = dist_setup(a.gpus)
+    names = sorted(WORKLOADS) if a.workload == "all" else [a.workload]
+
+    if a.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+        oracle.build()
+        for name in names:
+            wl = _cpu_only_workload(name, a)
+            run, sample_bytes, what = wl.cpu_sample()
+            for _ in range(a.warmup):
+                run()
+            t0 = time.perf_counter()
+            for _ in range(a.steps):
+                run()
+            dt = (time.perf_counter() - t0) / a.steps
+            v = sample_bytes / dt / 1e9
+            line = {"metric": METRIC, "value": round(v, 6), "unit": "GB/s", "n_gpus": a.gpus,
+                    "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(dt * 1e3, 4),
+                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                    "dtype": "f64", "data": "synthetic", "impl": "reference",
+                    "config": wl.config(),
+                    "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                     "sample": what},
+                    "e2e": {"value": round(v, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}
+            print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import stream_quantized_gemv_gb300 as pti
+    pti.build()
+    pti.lib()
+    peak, peak_kind = measured_peaks()
+    for name in names:
+        wl = WORKLOADS[name](a)
+        ms, clocks = time_gpu(wl, a.steps, a.warmup, world, local)
+        e2e_ms, h2d, d2h = time_e2e(wl, max(3, a.steps // 2), 2)
+        err = pti.device_error()
+        value = wl.step_bytes * world / (ms * 1e-3) / 1e9
+        per_launch_ms = ms / wl.launches_per_step
+        achieved = wl.launch_bytes / (per_launch_ms * 1e-3) / 1e9
+        traffic = recorded_traffic(wl.name)
+        line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+                "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 5),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": wl.dtype, "data": "synthetic (seeded; no model weights)",
+                "config": wl.config(),
+                "stream_tokens_per_s": round(wl.tokens_per_step * world / (ms * 1e-3), 2),
+                "hbm_frac": {"of_measured": round(value / world / peak, 4), "measured_gbs": peak,
+                             "peak_kind": peak_kind, "of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4)},
+                "roofline": {"bound": "hbm", "kernel": wl.dominant, "achieved": round(achieved, 2),
+                             "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                             "peak_kind": peak_kind, "traffic": traffic,
+                             "algorithmic_bytes_per_launch": wl.launch_bytes,
+                             "avg_launch_us": round(per_launch_ms * 1e3, 3)},
+                "e2e": {"value": round(wl.step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                        "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "gpu_launches": wl.launches_per_step * a.steps,
+                "clocks": clocks, "device_error": err}
+        if rank == 0 and world == 1 and not a.no_cpu_baseline:
+            import oracle
+            oracle.build()
+            v, what, dt = time_cpu(wl)
+            line["cpu_baseline"] = {"value": round(v, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                    "sample": what, "seconds_per_sample": round(dt, 4)}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        del wl
+        torch.cuda.empty_cache()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+class _CpuOnly:
+    pass
+
+
+def _cpu_only_workload(name, a):
+    """The workload's config and CPU sample without allocating device memory."""
+    cls = {"q8": Q8Pass, "twin": TwinPass, "verify": VerifyBatch}[name]
+    wl = cls.__new__(cls)
+    if name == "q8":
+        wl.rows, wl.cols, wl.n, wl.layers = a.rows or 17408, a.cols or 5120, a.n, a.layers or 16
+        wl.weight_bytes = wl.rows * (wl.cols // 32) * Q8_BLOCK
+    elif name == "twin":
+        wl.rows, wl.cols, wl.n, wl.layers = a.rows or 17408, a.cols or 5120, 2, a.layers or 8
+        wl.weight_bytes = wl.rows * (wl.cols // 32) * TWIN_BLOCK
+    else:
+        wl.steps, wl.n, wl.vocab, wl.p = 4096, 4, 151936, 0.6
+        wl.launch_bytes = wl.steps * wl.n * wl.vocab * 4
+    return wl
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,163 @@
+/*
+ * pti.h -- C ABI of the Packed Twin Inference hot path on NVIDIA GB300 (sm_103a).
+ *
+ * Packed Twin Inference is self-speculative decoding in which one weight load
+ * from HBM serves several token streams.  This library holds its hot path:
+ *
+ *   pti_q8_gemv_nstream   N-stream Q8 GEMV: one pass over a Q8 matrix computes
+ *                         y_s = W x_s for 1..4 activation vectors x_s.
+ *   pti_ssq_twin_gemv     SSQ "mode 16" twin GEMV: one pass over a packed twin
+ *                         matrix computes y_A = W_A x_A and y_B = W_B x_B.
+ *   pti_verify_greedy     greedy verify: per-stream argmax, guess == actual and
+ *                         the accepted-prefix length of every step.
+ *
+ * Sources are cited by page title and section:
+ *   [PTI-forum]  "Packed Twin Inference：无需草稿模型的推测解码新方案，实现2倍吞吐量提升"
+ *   [PTI-readme] "打包双子推理（PTI）"
+ *   [CS336-L10]  "推理（Inference）" (CS336 lecture 10 notes)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.  Every data pointer is DEVICE memory owned by the caller; the
+ *   library never frees or retains it.  No entry point allocates memory.  The
+ *   library keeps no per-call state; a device-side error word (see
+ *   pti_device_error) is the only global state.
+ * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   Every call only validates its arguments and enqueues work: PTI_OK means
+ *   "validated and launched", the results are ready when the stream reaches
+ *   that point.  Inputs are never modified.
+ * Errors.  Arguments are validated on the host before anything is enqueued;
+ *   a failed validation enqueues nothing.  A launch failure reported by the
+ *   CUDA runtime returns PTI_ERR_CUDA.  Kernels never trap or assert: a
+ *   pipeline wait that exceeds its time limit (which only a hardware fault can
+ *   cause) makes the kernel record a code in the device error word, skip its
+ *   remaining work and return.
+ * Layouts.  Little-endian byte layouts, matrices row-major:
+ *   Q8 block (34 bytes, 32 columns): [0..1] scale d as IEEE binary16,
+ *     [2..33] q[0..31] int8; weight = d * q.
+ *   SSQ twin block (68 bytes, 32 columns of two models A and B):
+ *     [0..1] scale_A binary16, [2..3] scale_B binary16, then 32 uint16 pw[i]
+ *     (bytes 4+2i, 5+2i) with model A's int8 in the high byte and model B's
+ *     int8 in the low byte ([PTI-forum] §"PTI的核心创新：SSQ打包技术").
+ *   A rows x cols matrix is rows consecutive rows of cols/32 blocks.
+ *   Activations and outputs are fp32, stream-major: x[s][k], y[s][r].
+ * Arithmetic.  fp32 with exact dequantisation (scale * q is formed exactly),
+ *   accumulation order fixed (results are bit-reproducible run to run); each
+ *   output stays within 1e-5 * sum_k |w_k x_k| of the exact value.
+ */
+#ifndef PTI_H
+#define PTI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *pti_stream_t; /* identical to cudaStream_t */
+
+typedef enum pti_status {
+    PTI_OK = 0,
+    PTI_ERR_NULL = 1,      /* a required pointer is NULL */
+    PTI_ERR_SHAPE = 2,     /* rows < 1, cols < 32, cols % 32 != 0, steps < 0, vocab < 1, too large */
+    PTI_ERR_NSTREAMS = 3,  /* n_streams outside [1, 4] (layers < 1 for the decode pass) */
+    PTI_ERR_ALIGN = 4,     /* a pointer is not aligned as documented */
+    PTI_ERR_ALIAS = 5,     /* an output overlaps an input or another output */
+    PTI_ERR_CUDA = 6,      /* the CUDA runtime reported an error (no device, launch failure) */
+    PTI_ERR_WORKSPACE = 7  /* workspace missing or smaller than required */
+} pti_status;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *pti_status_string(pti_status status);
+
+/*
+ * N-stream Q8 GEMV.
+ *   [PTI-readme] §"带宽分析：为什么会有开销": one kernel loads each weight
+ *   group once and forms the N dot products together, reading the N
+ *   activation vectors side by side and reducing all N streams in one pass.
+ *
+ *   w_q8       [rows][cols/32] Q8 blocks, 16-byte aligned.
+ *   rows, cols rows >= 1, cols >= 32, cols % 32 == 0, rows * cols < 2^40.
+ *   n_streams  1..4.
+ *   x          [n_streams][cols] fp32, 4-byte aligned.
+ *   y          [n_streams][rows] fp32 out, 4-byte aligned, overlapping neither
+ *              w_q8 nor x.
+ *   workspace  device scratch of at least pti_q8_gemv_workspace_bytes(rows,
+ *              cols, n_streams) bytes, 256-byte aligned, zero-filled before its
+ *              first use (it is left zero-filled by every call that completes);
+ *              may be NULL when that size is 0.  Calls that share a workspace
+ *              must be ordered (same stream or synchronised).
+ * Fast path when cols % 256 == 0: TMA-streamed, persistent, one pass over
+ * the weights; other shapes use a plain per-row kernel with the same results
+ * up to rounding order.
+ */
+size_t pti_q8_gemv_workspace_bytes(int64_t rows, int64_t cols, int n_streams);
+
+pti_status pti_q8_gemv_nstream(const void *w_q8, int64_t rows, int64_t cols, int n_streams,
+                               const float *x, float *y,
+                               void *workspace, size_t workspace_bytes,
+                               pti_stream_t stream);
+
+/*
+ * SSQ mode-16 twin GEMV.
+ *   [PTI-readme] §"与 SSQ（Side-by-Side Quantization）的关系": per uint16 pw,
+ *   wa = (int8)(pw >> 8), wb = (int8)(pw & 0xFF); acc_a += scale_a*wa*x_a[i],
+ *   acc_b += scale_b*wb*x_b[i]: one memory transaction, two compute streams.
+ *
+ *   w_twin     [rows][cols/32] twin blocks (68 bytes each), 16-byte aligned.
+ *   rows, cols as for the Q8 GEMV.
+ *   x_a, x_b   [cols] fp32 (A's and B's activations; may be the same pointer).
+ *   y_a, y_b   [rows] fp32 out; distinct, overlapping no input.
+ *   workspace  as for the Q8 GEMV, sized by pti_ssq_twin_gemv_workspace_bytes.
+ * Fast path when cols % 128 == 0.
+ */
+size_t pti_ssq_twin_gemv_workspace_bytes(int64_t rows, int64_t cols);
+
+pti_status pti_ssq_twin_gemv(const void *w_twin, int64_t rows, int64_t cols,
+                             const float *x_a, const float *x_b, float *y_a, float *y_b,
+                             void *workspace, size_t workspace_bytes,
+                             pti_stream_t stream);
+
+/*
+ * Greedy verify.
+ *   [PTI-readme] §"接受机制如何工作": stream 0 runs the model on the confirmed
+ *   token, stream s on the guess for position n+s; under greedy decoding the
+ *   guess fed to stream s+1 is accepted when it equals stream s's argmax, and
+ *   acceptance stops at the first mismatch (each step emits 1 + accept_len
+ *   tokens).  [PTI-forum] §"技术实现架构", step 3.
+ *
+ *   logits      [steps][n_streams][vocab] fp32, 4-byte aligned (16-byte
+ *               aligned rows take the vector path).  Precondition: no NaN.
+ *   guess       [steps][n_streams] int32; guess[t][0] is not read.
+ *   steps >= 0, n_streams in [1, 4], vocab in [1, 2^31 - 1].
+ *   argmax_out  [steps][n_streams] int32 out: the smallest index holding the
+ *               row's maximum (-0.0 and +0.0 compare equal).
+ *   match_out   [steps][n_streams-1] uint8 out, 1 when guess[t][s+1] ==
+ *               argmax[t][s]; may be NULL when n_streams == 1.
+ *   accept_len_out [steps] int32 out, the number of leading 1s of match, in
+ *               [0, n_streams - 1].
+ * steps == 0 enqueues nothing and returns PTI_OK.
+ */
+pti_status pti_verify_greedy(const float *logits, const int32_t *guess,
+                             int64_t steps, int n_streams, int64_t vocab,
+                             int32_t *argmax_out, uint8_t *match_out, int32_t *accept_len_out,
+                             pti_stream_t stream);
+
+/*
+ * Reads and clears the device error word of the current device (a blocking
+ * call: it synchronises the device).  0 means no kernel of this library has
+ * recorded an error since the last call; otherwise a bit set of
+ * PTI_DEVERR_* codes.  Returns PTI_OK or PTI_ERR_CUDA.
+ */
+#define PTI_DEVERR_FULL_TIMEOUT 0x1u  /* a consumer waited too long for a weight tile */
+#define PTI_DEVERR_EMPTY_TIMEOUT 0x2u /* the producer waited too long for a free slot */
+#define PTI_DEVERR_DRAIN_TIMEOUT 0x4u /* copies still in flight at exit after an error */
+pti_status pti_device_error(uint32_t *code_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PTI_H */

@@ -1,0 +1,174 @@
+"""Packed Twin Inference hot path on GB300: Python binding of ``libpti.so``.
+
+The compute lives in hand-written sm_103a CUDA kernels behind the C ABI of
+``include/pti.h``.  This module only marshals arguments: it turns torch device
+tensors into pointers, passes torch's current CUDA stream, allocates the
+(zero-filled, reusable) workspace the fast paths need, and raises ``PTIError``
+on a non-OK status.  There is no fallback: if ``libpti.so`` has not been built
+the import of the native library fails loudly.
+
+Functions (same names as the C ABI, without the ``pti_`` prefix):
+
+* ``q8_gemv_nstream(w, rows, cols, x)``      -> y [n][rows]
+* ``ssq_twin_gemv(w, rows, cols, x_a, x_b)``  -> (y_a, y_b)
+* ``verify_greedy(logits, guess)``            -> (argmax, match, accept_len)
+* ``device_error()``                          -> device error word (0 = none)
+* ``lib()``                                   -> the ctypes handle of the C ABI
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libpti.so")
+
+PTI_OK = 0
+STATUS_NAMES = {
+    0: "PTI_OK", 1: "PTI_ERR_NULL", 2: "PTI_ERR_SHAPE", 3: "PTI_ERR_NSTREAMS",
+    4: "PTI_ERR_ALIGN", 5: "PTI_ERR_ALIAS", 6: "PTI_ERR_CUDA", 7: "PTI_ERR_WORKSPACE",
+}
+
+
+class PTIError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compiles libpti.so in-tree (nvcc, sm_103a)."""
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The C ABI, with argument types declared.  Raises if the library is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"libpti.so is not built ({LIB_PATH}); run "
+                                  "stream_quantized_gemv_gb300.build() first")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I64, I, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+            L.pti_status_string.restype = ctypes.c_char_p
+            L.pti_status_string.argtypes = [I]
+            L.pti_q8_gemv_workspace_bytes.restype = SZ
+            L.pti_q8_gemv_workspace_bytes.argtypes = [I64, I64, I]
+            L.pti_q8_gemv_nstream.restype = I
+            L.pti_q8_gemv_nstream.argtypes = [P, I64, I64, I, P, P, P, SZ, P]
+            L.pti_ssq_twin_gemv_workspace_bytes.restype = SZ
+            L.pti_ssq_twin_gemv_workspace_bytes.argtypes = [I64, I64]
+            L.pti_ssq_twin_gemv.restype = I
+            L.pti_ssq_twin_gemv.argtypes = [P, I64, I64, P, P, P, P, P, SZ, P]
+            L.pti_verify_greedy.restype = I
+            L.pti_verify_greedy.argtypes = [P, P, I64, I, I64, P, P, P, P]
+            L.pti_device_error.restype = I
+            L.pti_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+            _lib = L
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != PTI_OK:
+        raise PTIError(status, what)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+_ws_cache: dict = {}
+
+
+def workspace(nbytes: int, device):
+    """A zero-filled device buffer of at least ``nbytes`` bytes, reused across
+    calls on the same device (every completed call leaves it zero-filled)."""
+    import torch
+    if nbytes == 0:
+        return None
+    dev = torch.device(device)
+    key = (dev.type, dev.index if dev.index is not None else torch.cuda.current_device())
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=dev)
+        _ws_cache[key] = buf
+    return buf
+
+
+def q8_gemv_workspace_bytes(rows: int, cols: int, n_streams: int) -> int:
+    return lib().pti_q8_gemv_workspace_bytes(rows, cols, n_streams)
+
+
+def ssq_twin_gemv_workspace_bytes(rows: int, cols: int) -> int:
+    return lib().pti_ssq_twin_gemv_workspace_bytes(rows, cols)
+
+
+def q8_gemv_nstream(w, rows: int, cols: int, x, y=None, ws=None, stream=None):
+    """y[s] = W x[s] for the n = x.shape[0] streams (1..4).  ``w``: uint8 Q8 bytes."""
+    import torch
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    n = x.shape[0]
+    if y is None:
+        y = torch.empty((n, rows), dtype=torch.float32, device=x.device)
+    need = q8_gemv_workspace_bytes(rows, cols, n)
+    if ws is None:
+        ws = workspace(need, x.device)
+    _check(lib().pti_q8_gemv_nstream(_ptr(w), rows, cols, n, _ptr(x), _ptr(y), _ptr(ws),
+                                     0 if ws is None else ws.numel() * ws.element_size(),
+                                     _stream(stream)), "pti_q8_gemv_nstream")
+    return y
+
+
+def ssq_twin_gemv(w, rows: int, cols: int, x_a, x_b, y_a=None, y_b=None, ws=None, stream=None):
+    """(y_A, y_B) = (W_A x_A, W_B x_B) from one packed twin matrix ``w`` (uint8)."""
+    import torch
+    if y_a is None:
+        y_a = torch.empty(rows, dtype=torch.float32, device=x_a.device)
+    if y_b is None:
+        y_b = torch.empty(rows, dtype=torch.float32, device=x_a.device)
+    need = ssq_twin_gemv_workspace_bytes(rows, cols)
+    if ws is None:
+        ws = workspace(need, x_a.device)
+    _check(lib().pti_ssq_twin_gemv(_ptr(w), rows, cols, _ptr(x_a), _ptr(x_b), _ptr(y_a), _ptr(y_b),
+                                   _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                                   _stream(stream)), "pti_ssq_twin_gemv")
+    return y_a, y_b
+
+
+def verify_greedy(logits, guess, argmax=None, match=None, accept=None, stream=None):
+    """Greedy verify of ``logits`` [steps][n][vocab] f32 against ``guess`` [steps][n] i32."""
+    import torch
+    steps, n, vocab = logits.shape
+    dev = logits.device
+    if argmax is None:
+        argmax = torch.empty((steps, n), dtype=torch.int32, device=dev)
+    if match is None:
+        match = torch.empty((steps, max(n - 1, 0)), dtype=torch.uint8, device=dev)
+    if accept is None:
+        accept = torch.empty(steps, dtype=torch.int32, device=dev)
+    match_ptr = _ptr(match) if n > 1 else 0
+    _check(lib().pti_verify_greedy(_ptr(logits), _ptr(guess), steps, n, vocab, _ptr(argmax), match_ptr,
+                                   _ptr(accept), _stream(stream)), "pti_verify_greedy")
+    return argmax, match, accept
+
+
+def device_error() -> int:
+    """Reads and clears the device error word (synchronises the device)."""
+    v = ctypes.c_uint32(0)
+    _check(lib().pti_device_error(ctypes.byref(v)), "pti_device_error")
+    return v.value

@@ -1,0 +1,236 @@
+// pti_device.cuh -- device-side building blocks shared by the sm_103a kernels:
+// mbarrier / TMA / PDL wrappers, time-bounded pipeline waits, packed f32x2
+// arithmetic and the exact int8 -> fp32 weight conversion.
+#pragma once
+
+#include <cstdint>
+#include <type_traits>
+
+#include <cuda_runtime.h>
+
+namespace pti {
+
+// A pipeline wait that has not completed after this long can only be a
+// hardware fault; the kernel then records an error and winds down.
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete.  Returns false if it
+// has not completed within kWaitTimeoutNs (or 2^30 polls), or, when
+// `abort_flag` is a shared-memory address other than 0, as soon as the 32-bit
+// word there becomes non-zero (another warp of the CTA recorded an error).
+__device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1; i < (1u << 30); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+      if (abort_flag != 0) {
+        uint32_t f;
+        asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(f) : "r"(abort_flag) : "memory");
+        if (f != 0) return false;
+      }
+    }
+  }
+  return false;
+}
+
+// ---------------------------------------------------------------------------
+// TMA (tiled 2-D tensor copy global -> shared, completion on an mbarrier)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int32_t c0, int32_t c1,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void *tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait_primary() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Named barrier among the first `threads` threads of the CTA (id 1..15).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory loads
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void lds_2x64(uint32_t addr, uint64_t &a, uint64_t &b) {
+  asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
+}
+
+__device__ __forceinline__ uint64_t lds64(uint32_t addr) {
+  uint64_t a;
+  asm volatile("ld.shared.b64 %0, [%1];" : "=l"(a) : "r"(addr));
+  return a;
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint16_t h;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(addr));
+  return h;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Packed f32x2 arithmetic (sm_100+): two independent fp32 lanes per
+// instruction, each rounded to nearest even exactly like the scalar op.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// ---------------------------------------------------------------------------
+// Exact int8 -> fp32 weight conversion.
+//
+// A weight byte b (two's complement q) is first XORed with 0x80, giving the
+// unsigned u = q + 128.  byte_to_magic() moves u into bits 8..15 of the fp32
+// pattern 0x4B000000 (2^23), which is the float f = 2^23 + 256 u exactly.
+// With the block scale d (a binary16, so 11 significant bits) and
+//   d' = d / 256,   c = -(2^15 + 2^7) d      (both exact in fp32)
+// one fused multiply-add gives f d' + c = (u - 128) d = q d, whose exact value
+// has at most 19 significant bits, so the single rounding of the FMA is exact.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float byte_to_magic(uint32_t word_xor80, uint32_t byte_index) {
+  // output bytes: [0] <- 0x00, [1] <- word.byte[k], [2] <- 0x00, [3] <- 0x4B
+  const uint32_t sel = 0x7504u | (byte_index << 4);
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(word_xor80), "r"(0x4B000000u), "r"(sel));
+  return __uint_as_float(r);
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t h16) {
+  float f;
+  asm("{\n\t.reg .b16 h;\n\tcvt.u16.u32 h, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(h16));
+  return f;
+}
+
+struct ScalePair {
+  uint64_t mul;  // {d/256, d/256}
+  uint64_t add;  // {-(2^15+2^7) d, -(2^15+2^7) d}
+};
+
+__device__ __forceinline__ ScalePair make_scale(uint32_t h16) {
+  const float d = half_bits_to_float(h16);
+  const float m = d * 0.00390625f;   // d / 256, exact
+  const float a = d * -32896.0f;     // -(2^15 + 2^7) d, exact (20 significant bits)
+  return ScalePair{pack2(m, m), pack2(a, a)};
+}
+
+// q*d for two weights held (XORed) in bytes k0 and k1 of the given words.
+__device__ __forceinline__ uint64_t dequant2(uint32_t w0, uint32_t k0, uint32_t w1, uint32_t k1,
+                                             const ScalePair &s) {
+  return ffma2(pack2(byte_to_magic(w0, k0), byte_to_magic(w1, k1)), s.mul, s.add);
+}
+
+// Compile-time loop helper.
+template <int I, int N, typename F>
+__device__ __forceinline__ void static_for(F &&f) {
+  if constexpr (I < N) {
+    f(std::integral_constant<int, I>{});
+    static_for<I + 1, N>(f);
+  }
+}
+
+}  // namespace pti

@@ -1,0 +1,106 @@
+"""The C-ABI library builds, loads and exports every entry point of include/pti.h,
+and its host-side argument checks reject bad calls before touching a GPU.
+
+Every call here fails validation, so no kernel is ever launched (safe with or
+without a GPU; fake pointer values are never dereferenced).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import stream_quantized_gemv_gb300 as pti
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    pti.build()
+    return pti.lib()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "pti.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pti_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_documented_entry_points():
+    names = _declared_functions()
+    for required in ("pti_q8_gemv_nstream", "pti_ssq_twin_gemv", "pti_verify_greedy",
+                     "pti_status_string", "pti_device_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for code, name in pti.STATUS_NAMES.items():
+        assert L.pti_status_string(code).decode().startswith(name)
+    assert L.pti_status_string(99).decode() == "PTI_ERR_UNKNOWN"
+
+
+def test_workspace_queries(L):
+    # fast paths need a workspace, plain paths do not, invalid shapes report 0
+    assert L.pti_q8_gemv_workspace_bytes(17408, 5120, 4) > 0
+    assert L.pti_q8_gemv_workspace_bytes(5120, 17408, 1) > 0
+    assert L.pti_q8_gemv_workspace_bytes(100, 96, 2) == 0
+    assert L.pti_q8_gemv_workspace_bytes(100, 256, 5) == 0
+    assert L.pti_q8_gemv_workspace_bytes(0, 256, 1) == 0
+    assert L.pti_ssq_twin_gemv_workspace_bytes(256, 512) > 0
+    assert L.pti_ssq_twin_gemv_workspace_bytes(256, 96) == 0
+    assert L.pti_q8_gemv_workspace_bytes(17408, 5120, 4) % 256 == 0
+
+
+FAKE = 0x7F0000000000  # 256-byte aligned, never dereferenced
+
+
+def _q8(L, w=FAKE, rows=128, cols=512, n=2, x=FAKE + (1 << 30), y=FAKE + (2 << 30),
+        ws=FAKE + (3 << 30), ws_bytes=1 << 24):
+    return L.pti_q8_gemv_nstream(w, rows, cols, n, x, y, ws, ws_bytes, None)
+
+
+def test_q8_validation(L):
+    assert _q8(L, w=None) == 1 and _q8(L, x=None) == 1 and _q8(L, y=None) == 1
+    assert _q8(L, rows=0) == 2 and _q8(L, cols=0) == 2 and _q8(L, cols=48) == 2
+    assert _q8(L, cols=16) == 2 and _q8(L, rows=1 << 32) == 2
+    assert _q8(L, n=0) == 3 and _q8(L, n=5) == 3
+    assert _q8(L, w=FAKE + 8) == 4 and _q8(L, x=FAKE + (1 << 30) + 2) == 4
+    assert _q8(L, y=FAKE + 4) == 5                      # y overlaps w
+    assert _q8(L, y=FAKE + (1 << 30) + 64) == 5          # y overlaps x
+    assert _q8(L, ws=None) == 7 and _q8(L, ws_bytes=16) == 7
+    assert _q8(L, ws=FAKE + (3 << 30) + 16) == 4
+    assert _q8(L, ws=FAKE + 256) == 5                    # workspace overlaps w
+
+
+def _twin(L, w=FAKE, rows=128, cols=512, xa=FAKE + (1 << 30), xb=FAKE + (1 << 30),
+          ya=FAKE + (2 << 30), yb=FAKE + (2 << 30) + 4096, ws=FAKE + (3 << 30), ws_bytes=1 << 24):
+    return L.pti_ssq_twin_gemv(w, rows, cols, xa, xb, ya, yb, ws, ws_bytes, None)
+
+
+def test_twin_validation(L):
+    assert _twin(L, w=None) == 1 and _twin(L, xb=None) == 1 and _twin(L, ya=None) == 1
+    assert _twin(L, rows=-1) == 2 and _twin(L, cols=33) == 2
+    assert _twin(L, w=FAKE + 4) == 4 and _twin(L, yb=FAKE + (2 << 30) + 4098) == 4
+    assert _twin(L, yb=FAKE + (2 << 30) + 8) == 5       # y_a and y_b overlap
+    assert _twin(L, ya=FAKE + 1024) == 5                # y_a overlaps w
+    assert _twin(L, ws=None) == 7
+
+
+def _verify(L, logits=FAKE, guess=FAKE + (1 << 34), steps=4, n=4, vocab=1000,
+            am=FAKE + (2 << 34), m=FAKE + (3 << 34), acc=FAKE + (4 << 34)):
+    return L.pti_verify_greedy(logits, guess, steps, n, vocab, am, m, acc, None)
+
+
+def test_verify_validation(L):
+    assert _verify(L, n=0) == 3 and _verify(L, n=5) == 3
+    assert _verify(L, steps=-1) == 2 and _verify(L, vocab=0) == 2 and _verify(L, vocab=1 << 31) == 2
+    assert _verify(L, logits=None) == 1 and _verify(L, m=None) == 1 and _verify(L, acc=None) == 1
+    assert _verify(L, logits=FAKE + 2) == 4 and _verify(L, am=FAKE + (2 << 34) + 1) == 4
+    assert _verify(L, am=FAKE + 64) == 5                 # argmax overlaps logits
+    assert _verify(L, acc=FAKE + (2 << 34) + 4) == 5     # accept overlaps argmax

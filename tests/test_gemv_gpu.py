@@ -1,0 +1,250 @@
+"""GPU parity of the N-stream Q8 GEMV and the SSQ twin GEMV against the fp64 oracle.
+
+Bar (per output element): |y_gpu - y_oracle| <= 1e-5 * sum_k |w_k x_k|, the
+oracle's exact bound.  Special cases whose result is exact in fp32 (one-hot x,
+integer weights and activations, zero weights, identical twins) are checked
+bit for bit.  Inputs come from the seeded generator (pti_synth) only.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pti_synth
+import stream_quantized_gemv_gb300 as pti
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    pti.build()
+    pti.lib()
+    yield
+    assert pti.device_error() == 0
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def assert_parity(y_gpu, y_ref, bound, what=""):
+    y_gpu = np.asarray(y_gpu, dtype=np.float64)
+    err = np.abs(y_gpu - y_ref)
+    bad = err > TOL * bound
+    if bad.any():
+        ratio = np.max(err / np.maximum(bound, 1e-300))
+        raise AssertionError(f"{what}: {bad.sum()} outputs off, max err/bound {ratio:.3g}")
+
+
+def tile_sample_rows(rows, rng):
+    """One row per 128-row tile (at a varying offset), plus the matrix ends."""
+    idx = {0, rows - 1}
+    for rb in range((rows + 127) // 128):
+        idx.add(min(rows - 1, rb * 128 + (rb * 37) % 128))
+    idx.update(rng.integers(0, rows, size=8).tolist())
+    return np.array(sorted(idx), dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
+# Q8, small and ragged shapes (fast path: cols % 256 == 0; plain path otherwise)
+# ---------------------------------------------------------------------------
+Q8_SHAPES = [(256, 512), (1, 256), (33, 256), (200, 768), (129, 1024), (1000, 2048),
+             (300, 96), (17, 544), (5, 32)]
+
+
+@pytest.mark.parametrize("rows,cols", Q8_SHAPES)
+@pytest.mark.parametrize("n", [1, 2, 3, 4])
+def test_q8_small_shapes_match_oracle(rows, cols, n):
+    w = pti_synth.q8_matrix(rows, cols, seed=rows * 7 + cols, tensor_id=n)
+    x = pti_synth.activations(n, cols, seed=rows + cols, tensor_id=n)
+    y_ref, bound = oracle.q8_gemv(w, rows, cols, x)
+    y = pti.q8_gemv_nstream(dev(w), rows, cols, dev(x)).cpu().numpy()
+    assert y.shape == (n, rows)
+    assert_parity(y, y_ref, bound, f"q8 {rows}x{cols} n={n}")
+
+
+def test_q8_is_bit_reproducible():
+    rows, cols = 1000, 2048
+    w = dev(pti_synth.q8_matrix(rows, cols, seed=1))
+    x = dev(pti_synth.activations(4, cols, seed=1))
+    a = pti.q8_gemv_nstream(w, rows, cols, x).clone()
+    b = pti.q8_gemv_nstream(w, rows, cols, x).clone()
+    assert torch.equal(a, b)
+
+
+def test_q8_one_hot_is_exact():
+    """x = e_j: every output is the single product d*q, exact in fp32."""
+    rows, cols = 300, 512
+    w = pti_synth.q8_matrix(rows, cols, seed=5)
+    for j in (0, 1, 31, 32, 255, 256, 511):
+        x = np.zeros((4, cols), np.float32)
+        x[0, j] = 1.0
+        x[1, (j + 1) % cols] = -1.0
+        x[2, j] = 2.0
+        x[3, (j + 100) % cols] = 0.5
+        y_ref, _ = oracle.q8_gemv(w, rows, cols, x)
+        y = pti.q8_gemv_nstream(dev(w), rows, cols, dev(x)).cpu().numpy().astype(np.float64)
+        assert np.array_equal(y, y_ref), j
+
+
+def test_q8_integer_case_is_exact():
+    """Scales 1.0, integer x in [-4, 4]: |y| < 2^24 so any order is exact."""
+    rows, cols = 257, 1024
+    w = pti_synth.q8_matrix(rows, cols, seed=9).reshape(-1, 34).copy()
+    w[:, 0], w[:, 1] = 0x00, 0x3C
+    w = w.reshape(-1)
+    xi = np.random.default_rng(2).integers(-4, 5, size=(4, cols)).astype(np.float32)
+    y_ref, _ = oracle.q8_gemv(w, rows, cols, xi)
+    y = pti.q8_gemv_nstream(dev(w), rows, cols, dev(xi)).cpu().numpy().astype(np.float64)
+    assert np.array_equal(y, y_ref)
+
+
+def test_q8_extreme_bytes_and_zero_weights():
+    rows, cols = 130, 512
+    w = pti_synth.q8_matrix(rows, cols, seed=3).reshape(-1, 34).copy()
+    w[0::3, 2:] = 0x80           # q = -128 (representable, outside the generator's range)
+    w[1::3, 2:] = 0x7F           # q = 127
+    w[2::3, 2:] = 0x00           # q = 0
+    w = w.reshape(-1)
+    x = pti_synth.activations(3, cols, seed=3)
+    y_ref, bound = oracle.q8_gemv(w, rows, cols, x)
+    y = pti.q8_gemv_nstream(dev(w), rows, cols, dev(x)).cpu().numpy()
+    assert_parity(y, y_ref, bound, "extreme bytes")
+
+
+# ---------------------------------------------------------------------------
+# Q8 at the configured full sizes, in the launch configuration the bench uses
+# ---------------------------------------------------------------------------
+@pytest.fixture(scope="module")
+def full_q8():
+    mats = {}
+    for rows, cols in ((17408, 5120), (5120, 17408)):
+        mats[(rows, cols)] = pti_synth.q8_matrix(rows, cols, seed=0, tensor_id=rows)
+    return mats
+
+
+@pytest.mark.parametrize("rows,cols", [(17408, 5120), (5120, 17408)])
+def test_q8_full_size_matches_oracle_on_every_tile(full_q8, rows, cols):
+    w_np = full_q8[(rows, cols)]
+    w = dev(w_np)
+    rng = np.random.default_rng(rows)
+    idx = tile_sample_rows(rows, rng)
+    for n in (1, 2, 3, 4):
+        x = pti_synth.activations(n, cols, seed=0, tensor_id=100 + n)
+        y = pti.q8_gemv_nstream(w, rows, cols, dev(x)).cpu().numpy()
+        assert np.isfinite(y).all()
+        y_ref, bound = oracle.q8_gemv(w_np, rows, cols, x, rows_idx=idx)
+        assert_parity(y[:, idx], y_ref, bound, f"q8 {rows}x{cols} n={n}")
+
+
+def test_q8_streams_are_independent_at_full_size(full_q8):
+    """Stream s of an N-stream call equals the 1-stream call on x[s] within the bar."""
+    rows, cols = 17408, 5120
+    w_np = full_q8[(rows, cols)]
+    w = dev(w_np)
+    x = dev(pti_synth.activations(4, cols, seed=5))
+    y4 = pti.q8_gemv_nstream(w, rows, cols, x).cpu().numpy()
+    idx = np.arange(0, rows, 97)
+    for s in range(4):
+        y1 = pti.q8_gemv_nstream(w, rows, cols, x[s:s + 1].contiguous()).cpu().numpy()
+        _, bound = oracle.q8_gemv(w_np, rows, cols, x[s:s + 1].cpu().numpy(), rows_idx=idx)
+        assert np.all(np.abs(y4[s, idx].astype(np.float64) - y1[0, idx]) <= 2 * TOL * bound[0])
+
+
+# ---------------------------------------------------------------------------
+# SSQ twin GEMV
+# ---------------------------------------------------------------------------
+def test_twin_256x512_seed0_matches_oracle():
+    """The 256 x 512 twin case (16 blocks per row, 68 bytes each), seed 0."""
+    rows, cols = 256, 512
+    w = pti_synth.twin_matrix(rows, cols, seed=0)
+    xa, xb = pti_synth.activations(2, cols, seed=0, tensor_id=1)
+    ya_ref, yb_ref, ba, bb = oracle.twin_gemv(w, rows, cols, xa, xb)
+    ya, yb = pti.ssq_twin_gemv(dev(w), rows, cols, dev(xa), dev(xb))
+    assert_parity(ya.cpu().numpy(), ya_ref, ba, "twin A")
+    assert_parity(yb.cpu().numpy(), yb_ref, bb, "twin B")
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 128), (3, 128), (130, 384), (129, 2048), (64, 96), (7, 224)])
+def test_twin_small_shapes_match_oracle(rows, cols):
+    w = pti_synth.twin_matrix(rows, cols, seed=rows + cols, tensor_id=2)
+    xa, xb = pti_synth.activations(2, cols, seed=cols, tensor_id=3)
+    ya_ref, yb_ref, ba, bb = oracle.twin_gemv(w, rows, cols, xa, xb)
+    ya, yb = pti.ssq_twin_gemv(dev(w), rows, cols, dev(xa), dev(xb))
+    assert_parity(ya.cpu().numpy(), ya_ref, ba, f"twin A {rows}x{cols}")
+    assert_parity(yb.cpu().numpy(), yb_ref, bb, f"twin B {rows}x{cols}")
+
+
+def test_twin_one_hot_is_exact_and_uses_high_byte_for_a():
+    rows, cols = 200, 256
+    w = pti_synth.twin_matrix(rows, cols, seed=4)
+    for j in (0, 1, 30, 31, 32, 127, 128, 255):
+        e = np.zeros(cols, np.float32)
+        e[j] = 1.0
+        f = np.zeros(cols, np.float32)
+        f[(j + 5) % cols] = -2.0
+        ya_ref, yb_ref, _, _ = oracle.twin_gemv(w, rows, cols, e, f)
+        ya, yb = pti.ssq_twin_gemv(dev(w), rows, cols, dev(e), dev(f))
+        assert np.array_equal(ya.cpu().numpy().astype(np.float64), ya_ref), j
+        assert np.array_equal(yb.cpu().numpy().astype(np.float64), yb_ref), j
+
+
+@pytest.fixture(scope="module")
+def full_twin():
+    return {(r, c): pti_synth.twin_matrix(r, c, seed=0, tensor_id=r) for r, c in ((17408, 5120), (5120, 17408))}
+
+
+@pytest.mark.parametrize("rows,cols", [(17408, 5120), (5120, 17408)])
+def test_twin_full_size_matches_oracle_on_every_tile(full_twin, rows, cols):
+    w_np = full_twin[(rows, cols)]
+    xa, xb = pti_synth.activations(2, cols, seed=0, tensor_id=200)
+    ya, yb = pti.ssq_twin_gemv(dev(w_np), rows, cols, dev(xa), dev(xb))
+    idx = tile_sample_rows(rows, np.random.default_rng(rows + 1))
+    ya_ref, yb_ref, ba, bb = oracle.twin_gemv(w_np, rows, cols, xa, xb, rows_idx=idx)
+    assert_parity(ya.cpu().numpy()[idx], ya_ref, ba, "twin A full")
+    assert_parity(yb.cpu().numpy()[idx], yb_ref, bb, "twin B full")
+
+
+@pytest.mark.parametrize("rows,cols", [(17408, 5120), (5120, 17408)])
+def test_identical_twins_give_identical_outputs(rows, cols):
+    """A == B and x_A == x_B: y_A == y_B bit for bit, and both match the oracle."""
+    w_np = pti_synth.twin_matrix(rows, cols, seed=1, tensor_id=7, identical=True)
+    x = pti_synth.activations(1, cols, seed=1, tensor_id=8)[0]
+    xd = dev(x)
+    ya, yb = pti.ssq_twin_gemv(dev(w_np), rows, cols, xd, xd)
+    assert torch.equal(ya, yb)
+    idx = np.arange(0, rows, 211)
+    ya_ref, _, ba, _ = oracle.twin_gemv(w_np, rows, cols, x, x, rows_idx=idx)
+    assert_parity(ya.cpu().numpy()[idx], ya_ref, ba, "identical twins")
+
+
+def test_twin_matches_q8_on_unpacked_models():
+    """Cross-kernel: twin(T, x_a, x_b) agrees with the Q8 GEMV of each unpacked model."""
+    rows, cols = 520, 1024
+    t = pti_synth.twin_matrix(rows, cols, seed=12)
+    qa, qb = oracle.twin_unpack(t)
+    xa, xb = pti_synth.activations(2, cols, seed=12)
+    ya, yb = pti.ssq_twin_gemv(dev(t), rows, cols, dev(xa), dev(xb))
+    ra = pti.q8_gemv_nstream(dev(qa), rows, cols, dev(xa[None])).cpu().numpy()[0]
+    rb = pti.q8_gemv_nstream(dev(qb), rows, cols, dev(xb[None])).cpu().numpy()[0]
+    _, _, ba, bb = oracle.twin_gemv(t, rows, cols, xa, xb)
+    assert np.all(np.abs(ya.cpu().numpy().astype(np.float64) - ra) <= 2 * TOL * ba)
+    assert np.all(np.abs(yb.cpu().numpy().astype(np.float64) - rb) <= 2 * TOL * bb)
+
+
+def test_workspace_reuse_across_calls():
+    """Every call leaves the workspace ready for the next one: three calls in a
+    row on one fresh zeroed workspace all match the oracle."""
+    rows, cols = 1000, 2048
+    need = pti.q8_gemv_workspace_bytes(rows, cols, 4)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    w_np = pti_synth.q8_matrix(rows, cols, seed=2)
+    w = dev(w_np)
+    for k in range(3):
+        x = pti_synth.activations(4, cols, seed=20 + k)
+        y = pti.q8_gemv_nstream(w, rows, cols, dev(x), ws=ws).cpu().numpy()
+        y_ref, bound = oracle.q8_gemv(w_np, rows, cols, x)
+        assert_parity(y, y_ref, bound, f"call {k}")
