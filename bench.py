@@ -117,7 +117,7 @@ class ClockSampler:
         sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
         smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
         loaded = sorted(sm)[len(sm) // 2:] if sm else []
         return {"sm_mhz": statistics.median(loaded) if loaded else None,
                 "sm_max_mhz": max(smax) if smax else None,
@@ -182,7 +182,7 @@ class Q8Pass:
         self.launches_per_step = layers
         self.tokens_per_step = n
         self.dominant = "gemv_tma_kernel<Q8,%d>" % n
-        self.dtype = "f32 (int8 weights with binary16 block scales, exact dequantisation)"
+        self.dtype = "f32"
 
     def step(self, x=None, y=None):
         x = self.x if x is None else x
@@ -237,7 +237,7 @@ class TwinPass(Q8Pass):
         self.launches_per_step = layers
         self.tokens_per_step = 2
         self.dominant = "gemv_tma_kernel<Twin>"
-        self.dtype = "f32 (two int8 models packed per uint16, binary16 scales, exact dequantisation)"
+        self.dtype = "f32"
 
     def step(self, x=None, y=None):
         x = self.x if x is None else x
@@ -282,7 +282,7 @@ class VerifyBatch(Q8Pass):
         self.launches_per_step = 1
         self.tokens_per_step = steps * n
         self.dominant = "verify_greedy_kernel"
-        self.dtype = "f32 compare, int32 indices"
+        self.dtype = "f32"
         self.x = self.logits
         self.y = self.out[2]
 

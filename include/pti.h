@@ -86,12 +86,14 @@ const char *pti_status_string(pti_status status);
  *              w_q8 nor x.
  *   workspace  device scratch of at least pti_q8_gemv_workspace_bytes(rows,
  *              cols, n_streams) bytes, 256-byte aligned, zero-filled before its
- *              first use (it is left zero-filled by every call that completes);
+ *              first use (every call that completes leaves all of it zero-filled
+ *              again, so one workspace serves calls of any shape and stream
+ *              count);
  *              may be NULL when that size is 0.  Calls that share a workspace
  *              must be ordered (same stream or synchronised).
- * Fast path when cols % 256 == 0: TMA-streamed, persistent, one pass over
- * the weights; other shapes use a plain per-row kernel with the same results
- * up to rounding order.
+ * Fast path when cols % 256 == 0 and x is 16-byte aligned: TMA-streamed,
+ * persistent, one pass over the weights; other calls use a plain per-row
+ * kernel with the same bound on the error (a different rounding order).
  */
 size_t pti_q8_gemv_workspace_bytes(int64_t rows, int64_t cols, int n_streams);
 
@@ -111,7 +113,7 @@ pti_status pti_q8_gemv_nstream(const void *w_q8, int64_t rows, int64_t cols, int
  *   x_a, x_b   [cols] fp32 (A's and B's activations; may be the same pointer).
  *   y_a, y_b   [rows] fp32 out; distinct, overlapping no input.
  *   workspace  as for the Q8 GEMV, sized by pti_ssq_twin_gemv_workspace_bytes.
- * Fast path when cols % 128 == 0.
+ * Fast path when cols % 128 == 0 and x_a, x_b are 16-byte aligned.
  */
 size_t pti_ssq_twin_gemv_workspace_bytes(int64_t rows, int64_t cols);
 
@@ -138,7 +140,8 @@ pti_status pti_ssq_twin_gemv(const void *w_twin, int64_t rows, int64_t cols,
  *               argmax[t][s]; may be NULL when n_streams == 1.
  *   accept_len_out [steps] int32 out, the number of leading 1s of match, in
  *               [0, n_streams - 1].
- * steps == 0 enqueues nothing and returns PTI_OK.
+ * steps == 0 enqueues nothing and returns PTI_OK (the pointers are not
+ * checked, since nothing is read or written).
  */
 pti_status pti_verify_greedy(const float *logits, const int32_t *guess,
                              int64_t steps, int n_streams, int64_t vocab,

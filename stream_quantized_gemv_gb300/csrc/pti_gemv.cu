@@ -19,13 +19,16 @@
 //    last CTA to finish them (an atomic ticket per tile, partials in a
 //    caller-supplied workspace, summed in a fixed CTA order).
 //  * One producer warp issues the TMA copies into a 4-stage ring guarded by
-//    mbarriers; 15 consumer warps compute.  Consumer warp w owns chunk w of
-//    every unit (chunks 15 and 16 rotate over the warps), and lane l owns rows
-//    l, l+32, l+64, l+96 of the tile: each lane reads its chunk with one
-//    aligned, bank-conflict-free 16-byte shared load per row.
+//    mbarriers; 16 consumer warps compute.  Lane l of a consumer task owns two
+//    rows of the tile and reads its 16-byte chunk of each with one aligned,
+//    bank-conflict-free shared load.  The 17 chunk positions need 17
+//    specialised code bodies; to keep each scheduler's instruction working set
+//    small, scheduler k owns chunks k, k+4, k+8, k+12 (chunk 16 rotates over
+//    the schedulers from unit to unit) and its four warps split each owned
+//    chunk into two 64-row halves.
 //  * The activations of the unit's columns are staged once per CTA segment in
 //    shared memory as float2 column pairs; every warp reads them with
-//    broadcast loads and reuses them for its 128 rows, so activation traffic
+//    broadcast loads and reuses them for its 64 rows, so activation traffic
 //    does not grow with the number of row tiles (the L2 thrash the pages
 //    diagnose for the per-row-block design).
 //  * Dequantisation is exact (see pti_device.cuh); products use packed
@@ -51,12 +54,10 @@ namespace {
 
 constexpr int kSBBytes = 272;                          // super-block bytes (17 chunks of 16)
 constexpr int kRowsPerTile = 128;                      // rows per unit
-constexpr int kSlots = kRowsPerTile / 32;              // rows per lane
-constexpr int kStages = 4;
+constexpr int kMaxStages = 6;
 constexpr int kStageBytes = kRowsPerTile * kSBBytes;   // 34816
 constexpr int kMaxGrid = 320;
 constexpr int kSmemOptin = 232448;                     // 227 KB per CTA
-constexpr int kBarBytes = 2 * kStages * 8 + 16;        // full[], empty[], two flag words
 constexpr uint32_t kBarConsumers = 1;                  // named barrier of the consumer warps
 
 __device__ unsigned int g_device_error = 0;
@@ -68,21 +69,28 @@ struct Traits;
 template <int N>
 struct Traits<Fmt::Q8, N> {
   static constexpr int kOut = N;                   // output vectors
-  static constexpr int kNS = (N == 3) ? 4 : N;     // float2 slots per staged column pair
-  // 4 streams need ~136 registers per thread: 14 consumer warps + 1 producer
-  // warp keep the CTA within the 64K-register file.
-  static constexpr int kWarps = (N == 4) ? 14 : 15;
+  static constexpr int kWarps = 16;   // consumer warps (4 per scheduler)
   static constexpr int kColsPerSB = 256;
-  static constexpr int kXBytesPerSB = (kColsPerSB / 2) * kNS * 8;
+  static constexpr int kXStreams = N;
   static constexpr int kBlockBytes = 34;
 };
 template <int N>
 struct Traits<Fmt::Twin, N> {
   static constexpr int kOut = 2;
-  static constexpr int kWarps = 15;
+  static constexpr int kWarps = 16;
   static constexpr int kColsPerSB = 128;
-  static constexpr int kXBytesPerSB = (kColsPerSB / 2) * 16;
+  static constexpr int kXStreams = 2;
   static constexpr int kBlockBytes = 68;
+};
+
+// One pipeline stage: the 128 x 272-byte weight tile followed by the unit's
+// activations, stream-major (kXStreams rows of kColsPerSB floats).
+template <Fmt F, int N>
+struct Stage {
+  static constexpr int kXStreamBytes = Traits<F, N>::kColsPerSB * 4;
+  static constexpr int kXBytes = Traits<F, N>::kXStreams * kXStreamBytes;
+  static constexpr int kBytes = ((kStageBytes + kXBytes) + 1023) / 1024 * 1024;
+  static constexpr int kRedBytes = 2 * Traits<F, N>::kWarps * Traits<F, N>::kOut * 64 * 4;
 };
 
 struct GemvArgs {
@@ -93,242 +101,204 @@ struct GemvArgs {
   float *part;      // workspace: [grid][2 slots][kOut][128] partial sums
   unsigned int *tickets;  // workspace: [n_rb] arrival counters (zero between calls)
   int64_t rows, cols, units;
-  int32_t n_sb, n_rb, grid, xw_sb;
-  uint32_t x_region_bytes;
+  int32_t n_sb, n_rb, grid, stages;
 };
 
-// ---------------------------------------------------------------------------
-// Chunk geometry (compile time).
-// Q8 super-block: block b occupies bytes [34b, 34b+34): scale at 34b, q[i] at
-// 34b+2+i (column 32b+i).  A 16-byte chunk's bytes pair up as (2m, 2m+1); the
-// two bytes of a pair are always both scale bytes or both weights of one block.
-// ---------------------------------------------------------------------------
-struct Q8Geom {
-  static constexpr int absb(int c, int p) { return 16 * c + p; }
-  static constexpr bool is_scale(int c, int p) { return absb(c, p) % 34 < 2; }
-  static constexpr int block(int c, int p) { return absb(c, p) / 34; }
-  static constexpr int col(int c, int p) { return 32 * block(c, p) + absb(c, p) % 34 - 2; }
-  static constexpr int first_pair(int c) {
-    for (int m = 0; m < 8; ++m)
-      if (!is_scale(c, 2 * m)) return m;
-    return -1;
-  }
-  static constexpr int first_block(int c) { return block(c, 2 * first_pair(c)); }
-  static constexpr int last_block(int c) {
-    int b = -1;
-    for (int m = 0; m < 8; ++m)
-      if (!is_scale(c, 2 * m)) b = block(c, 2 * m);
-    return b;
-  }
-  // byte offset of block b's scale inside chunk c, or -1
-  static constexpr int scale_in_chunk(int c, int b) {
-    return (34 * b - 16 * c >= 0 && 34 * b - 16 * c < 16) ? 34 * b - 16 * c : -1;
-  }
+// Rows handled by one warp task: lane l owns rows 64h + l and 64h + 32 + l of
+// the tile (h = the task's half).
+constexpr int kTaskSlots = 2;
+
+// Where a 16-byte chunk's weights sit.  Chunks come in a few structural
+// classes: `cls` = -1 when the chunk holds no scale (all its bytes are weights
+// of block b0), else the index of the byte pair holding the next block's scale
+// (Q8: 0..7; twin: the word index 0..3).  The generic parameters are the byte
+// offset of the chunk, the offset of block b0's scale in the row, and the
+// column pair of the chunk's first weight pair (`cpbase`).
+struct ChunkParams {
+  int cls;
+  uint32_t choff;     // 16 * c
+  uint32_t scale_off; // byte offset of block b0's scale within the super-block row
+  uint32_t cpbase;    // column pair (within the super-block) of pair 0
 };
 
-// Twin super-block: 68 words; block b = words [17b, 17b+17): word 17b holds
-// scale_A (low half) and scale_B (high half), word 17b+1+j holds columns
-// 32b+2j and 32b+2j+1 as bytes [B_2j, A_2j, B_2j+1, A_2j+1].
-struct TwinGeom {
-  static constexpr int word(int c, int j) { return 4 * c + j; }
-  static constexpr int block(int c, int j) { return word(c, j) / 17; }
-  static constexpr bool is_scale(int c, int j) { return word(c, j) % 17 == 0; }
-  static constexpr int colpair(int c, int j) { return 16 * block(c, j) + word(c, j) % 17 - 1; }
-  static constexpr int first_word(int c) {
-    for (int j = 0; j < 4; ++j)
-      if (!is_scale(c, j)) return j;
-    return -1;
+__device__ __forceinline__ ChunkParams q8_chunk_params(int c) {
+  ChunkParams p;
+  p.choff = 16u * c;
+  if (c <= 14 && (c & 1) == 0) {  // the scale of block c/2 sits at pair (16c - 34(c/2)) / 2 = c/2
+    p.cls = c / 2;
+    const int b0 = c / 2 > 0 ? c / 2 - 1 : 0;
+    p.scale_off = 34u * b0;
+    p.cpbase = 15u * (c / 2);
+  } else {
+    const int b0 = (16 * c) / 34;
+    p.cls = -1;
+    p.scale_off = 34u * b0;
+    p.cpbase = static_cast<uint32_t>((32 * b0 + (16 * c) % 34 - 2) / 2);
   }
-  static constexpr int first_block(int c) { return block(c, first_word(c)); }
-  static constexpr int last_block(int c) {
-    int b = -1;
-    for (int j = 0; j < 4; ++j)
-      if (!is_scale(c, j)) b = block(c, j);
-    return b;
+  return p;
+}
+
+__device__ __forceinline__ ChunkParams twin_chunk_params(int c) {
+  ChunkParams p;
+  p.choff = 16u * c;
+  if ((c & 3) == 0 && c <= 12) {  // chunk c holds the scale word of block c/4 at word c/4
+    p.cls = c / 4;
+    const int b0 = c / 4 > 0 ? c / 4 - 1 : 0;
+    p.scale_off = 68u * b0;
+    p.cpbase = 15u * (c / 4);
+  } else {
+    const int b0 = (4 * c) / 17;
+    p.cls = -1;
+    p.scale_off = 68u * b0;
+    p.cpbase = static_cast<uint32_t>(16 * b0 + (4 * c) % 17 - 1);
   }
-  static constexpr int scale_in_chunk(int c, int b) {
-    return (17 * b - 4 * c >= 0 && 17 * b - 4 * c < 4) ? 17 * b - 4 * c : -1;
-  }
-};
+  return p;
+}
 
 template <int I>
-__device__ __forceinline__ uint32_t word_of(const uint4 &w) {
+__device__ __forceinline__ uint32_t word_at(const uint4 &w) {
   if constexpr (I == 0) return w.x;
   else if constexpr (I == 1) return w.y;
   else if constexpr (I == 2) return w.z;
   else return w.w;
 }
 
-template <int C, int B>
-__device__ __forceinline__ uint32_t q8_scale_bits(const uint4 &w, uint32_t row_addr) {
-  constexpr int o = Q8Geom::scale_in_chunk(C, B);
-  if constexpr (o >= 0) {
-    const uint32_t wd = word_of<o / 4>(w);
-    return (o % 4 == 0) ? (wd & 0xFFFFu) : (wd >> 16);
-  } else {
-    return lds_u16(row_addr + 34 * B);
+// One Q8 chunk of class K for the lane's two rows of half h.  Byte pair m of
+// the chunk holds weight columns cpbase + m (pairs before the scale) or
+// cpbase + m - 1 (pairs after it).
+template <int N, int K>
+__device__ __forceinline__ void q8_body(const uint8_t *tile, const ChunkParams &cp, const uint8_t *xsb,
+                                        uint32_t lane, uint32_t half, uint64_t (&acc)[kTaskSlots][N]) {
+  constexpr int M0 = (K == 0) ? 1 : 0;  // first weight pair
+  uint32_t wx[kTaskSlots][4];
+  ScalePair s_lo[kTaskSlots], s_hi[kTaskSlots];
+#pragma unroll
+  for (int r = 0; r < kTaskSlots; ++r) {
+    const uint8_t *row = tile + (half * 64 + r * 32 + lane) * kSBBytes;
+    const uint4 w = *reinterpret_cast<const uint4 *>(row + cp.choff);
+    if constexpr (K != 0) s_lo[r] = make_scale(*reinterpret_cast<const uint16_t *>(row + cp.scale_off));
+    if constexpr (K >= 0) {
+      const uint32_t wd = word_at<K / 2>(w);
+      s_hi[r] = make_scale((K & 1) ? (wd >> 16) : (wd & 0xFFFFu));
+    }
+    wx[r][0] = w.x ^ 0x80808080u;
+    wx[r][1] = w.y ^ 0x80808080u;
+    wx[r][2] = w.z ^ 0x80808080u;
+    wx[r][3] = w.w ^ 0x80808080u;
   }
-}
-
-template <int C, int B>
-__device__ __forceinline__ uint32_t twin_scale_word(const uint4 &w, uint32_t row_addr) {
-  constexpr int j = TwinGeom::scale_in_chunk(C, B);
-  if constexpr (j >= 0) {
-    return word_of<j>(w);
-  } else {
-    return lds32(row_addr + 68 * B);
-  }
-}
-
-// One Q8 chunk C of one unit, for the lane's 4 rows.
-template <int N, int C>
-__device__ __forceinline__ void q8_chunk(uint32_t tile, uint32_t xsb, uint32_t lane,
-                                         uint64_t (&acc)[kSlots][N]) {
-  using T = Traits<Fmt::Q8, N>;
-  constexpr int B0 = Q8Geom::first_block(C);
-  constexpr int B1 = Q8Geom::last_block(C);
-  constexpr int M0 = Q8Geom::first_pair(C);
-  uint64_t xp[8][N];
+  const uint8_t *xc = xsb + cp.cpbase * 8;
+  uint64_t p[kTaskSlots][N];
   static_for<0, 8>([&](auto mc) {
     constexpr int m = decltype(mc)::value;
-    if constexpr (!Q8Geom::is_scale(C, 2 * m)) {
-      constexpr int cp = Q8Geom::col(C, 2 * m) / 2;
-      const uint32_t a = xsb + cp * T::kNS * 8;
-      if constexpr (T::kNS == 4) {
-        uint64_t t2, t3;
-        lds_2x64(a, xp[m][0], xp[m][1]);
-        lds_2x64(a + 16, t2, t3);
-        if constexpr (N >= 3) xp[m][2] = t2;
-        if constexpr (N == 4) xp[m][3] = t3;
-      } else if constexpr (T::kNS == 2) {
-        lds_2x64(a, xp[m][0], xp[m][1]);
-      } else {
-        xp[m][0] = lds64(a);
-      }
-    }
-  });
+    if constexpr (m != K) {
+      constexpr int off = (K >= 0 && m > K) ? m - 1 : m;
+      uint64_t xv[N];
 #pragma unroll
-  for (int r = 0; r < kSlots; ++r) {
-    const uint32_t row_addr = tile + (r * 32 + lane) * kSBBytes;
-    const uint4 w = lds128(row_addr + 16 * C);
-    const uint32_t wx[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u,
-                            w.w ^ 0x80808080u};
-    const ScalePair s0 = make_scale(q8_scale_bits<C, B0>(w, row_addr));
-    ScalePair s1 = s0;
-    if constexpr (B1 != B0) s1 = make_scale(q8_scale_bits<C, B1>(w, row_addr));
-    uint64_t p[N];
-    static_for<0, 8>([&](auto mc) {
-      constexpr int m = decltype(mc)::value;
-      if constexpr (!Q8Geom::is_scale(C, 2 * m)) {
-        constexpr int k = 2 * m;
-        const ScalePair &sc = (Q8Geom::block(C, k) == B0) ? s0 : s1;
-        const uint64_t wq = dequant2(wx[k / 4], k % 4, wx[k / 4], k % 4 + 1, sc);
+      for (int st = 0; st < N; ++st)
+        xv[st] = *reinterpret_cast<const uint64_t *>(xc + st * Stage<Fmt::Q8, N>::kXStreamBytes + off * 8);
+#pragma unroll
+      for (int r = 0; r < kTaskSlots; ++r) {
+        const ScalePair &sc = (K < 0 || m < K) ? s_lo[r] : s_hi[r];
+        const uint64_t wq = dequant2(wx[r][m / 2], (2 * m) % 4, wx[r][m / 2], (2 * m) % 4 + 1, sc);
         static_for<0, N>([&](auto sc_) {
           constexpr int s = decltype(sc_)::value;
-          if constexpr (m == M0) p[s] = fmul2(wq, xp[m][s]);
-          else p[s] = ffma2(wq, xp[m][s], p[s]);
+          if constexpr (m == M0) p[r][s] = fmul2(wq, xv[s]);
+          else p[r][s] = ffma2(wq, xv[s], p[r][s]);
         });
       }
-    });
-    static_for<0, N>([&](auto sc_) {
-      constexpr int s = decltype(sc_)::value;
-      acc[r][s] = fadd2(acc[r][s], p[s]);
-    });
-  }
-}
-
-// One twin chunk C of one unit, for the lane's 4 rows.
-template <int C>
-__device__ __forceinline__ void twin_chunk(uint32_t tile, uint32_t xsb, uint32_t lane,
-                                           uint64_t (&acc)[kSlots][2]) {
-  constexpr int B0 = TwinGeom::first_block(C);
-  constexpr int B1 = TwinGeom::last_block(C);
-  constexpr int J0 = TwinGeom::first_word(C);
-  uint64_t xa[4], xb[4];
-  static_for<0, 4>([&](auto jc) {
-    constexpr int j = decltype(jc)::value;
-    if constexpr (!TwinGeom::is_scale(C, j)) lds_2x64(xsb + TwinGeom::colpair(C, j) * 16, xa[j], xb[j]);
+    }
   });
 #pragma unroll
-  for (int r = 0; r < kSlots; ++r) {
-    const uint32_t row_addr = tile + (r * 32 + lane) * kSBBytes;
-    const uint4 w = lds128(row_addr + 16 * C);
-    const uint32_t sw0 = twin_scale_word<C, B0>(w, row_addr);
-    const ScalePair sa0 = make_scale(sw0 & 0xFFFFu), sb0 = make_scale(sw0 >> 16);
-    ScalePair sa1 = sa0, sb1 = sb0;
-    if constexpr (B1 != B0) {
-      const uint32_t sw1 = twin_scale_word<C, B1>(w, row_addr);
-      sa1 = make_scale(sw1 & 0xFFFFu);
-      sb1 = make_scale(sw1 >> 16);
+  for (int r = 0; r < kTaskSlots; ++r)
+    static_for<0, N>([&](auto sc_) {
+      constexpr int s = decltype(sc_)::value;
+      acc[r][s] = fadd2(acc[r][s], p[r][s]);
+    });
+}
+
+// One twin chunk of class J for the lane's two rows of half h.  Word j of the
+// chunk holds column pair cpbase + j (before the scale word) or cpbase + j - 1.
+template <int N, int J>
+__device__ __forceinline__ void twin_body(const uint8_t *tile, const ChunkParams &cp, const uint8_t *xsb,
+                                          uint32_t lane, uint32_t half, uint64_t (&acc)[kTaskSlots][2]) {
+  constexpr int J0 = (J == 0) ? 1 : 0;
+  uint4 w[kTaskSlots];
+  ScalePair sa_lo[kTaskSlots], sb_lo[kTaskSlots], sa_hi[kTaskSlots], sb_hi[kTaskSlots];
+#pragma unroll
+  for (int r = 0; r < kTaskSlots; ++r) {
+    const uint8_t *row = tile + (half * 64 + r * 32 + lane) * kSBBytes;
+    w[r] = *reinterpret_cast<const uint4 *>(row + cp.choff);
+    if constexpr (J != 0) {
+      const uint32_t sw = *reinterpret_cast<const uint32_t *>(row + cp.scale_off);
+      sa_lo[r] = make_scale(sw & 0xFFFFu);
+      sb_lo[r] = make_scale(sw >> 16);
     }
-    uint64_t pa, pb;
-    static_for<0, 4>([&](auto jc) {
-      constexpr int j = decltype(jc)::value;
-      if constexpr (!TwinGeom::is_scale(C, j)) {
-        const bool first_blk = TwinGeom::block(C, j) == B0;
-        const ScalePair &sa = first_blk ? sa0 : sa1;
-        const ScalePair &sb = first_blk ? sb0 : sb1;
-        const uint32_t wxj = word_of<j>(w) ^ 0x80808080u;
-        const uint64_t wa = dequant2(wxj, 1, wxj, 3, sa);  // model A: high bytes
-        const uint64_t wb = dequant2(wxj, 0, wxj, 2, sb);  // model B: low bytes
+    if constexpr (J >= 0) {
+      const uint32_t sw = word_at<J>(w[r]);
+      sa_hi[r] = make_scale(sw & 0xFFFFu);
+      sb_hi[r] = make_scale(sw >> 16);
+    }
+  }
+  const uint8_t *xc = xsb + cp.cpbase * 8;
+  uint64_t pa[kTaskSlots], pb[kTaskSlots];
+  static_for<0, 4>([&](auto jc) {
+    constexpr int j = decltype(jc)::value;
+    if constexpr (j != J) {
+      constexpr int off = (J >= 0 && j > J) ? j - 1 : j;
+      const uint64_t xa = *reinterpret_cast<const uint64_t *>(xc + off * 8);
+      const uint64_t xb = *reinterpret_cast<const uint64_t *>(xc + Stage<Fmt::Twin, N>::kXStreamBytes + off * 8);
+      constexpr bool lo = (J < 0 || j < J);
+#pragma unroll
+      for (int r = 0; r < kTaskSlots; ++r) {
+        const uint32_t wxj = word_at<j>(w[r]) ^ 0x80808080u;
+        const uint64_t wa = dequant2(wxj, 1, wxj, 3, lo ? sa_lo[r] : sa_hi[r]);  // model A: high bytes
+        const uint64_t wb = dequant2(wxj, 0, wxj, 2, lo ? sb_lo[r] : sb_hi[r]);  // model B: low bytes
         if constexpr (j == J0) {
-          pa = fmul2(wa, xa[j]);
-          pb = fmul2(wb, xb[j]);
+          pa[r] = fmul2(wa, xa);
+          pb[r] = fmul2(wb, xb);
         } else {
-          pa = ffma2(wa, xa[j], pa);
-          pb = ffma2(wb, xb[j], pb);
+          pa[r] = ffma2(wa, xa, pa[r]);
+          pb[r] = ffma2(wb, xb, pb[r]);
         }
       }
-    });
-    acc[r][0] = fadd2(acc[r][0], pa);
-    acc[r][1] = fadd2(acc[r][1], pb);
+    }
+  });
+#pragma unroll
+  for (int r = 0; r < kTaskSlots; ++r) {
+    acc[r][0] = fadd2(acc[r][0], pa[r]);
+    acc[r][1] = fadd2(acc[r][1], pb[r]);
   }
 }
 
-template <Fmt F, int N, int C>
-__device__ __forceinline__ void chunk_body(uint32_t tile, uint32_t xsb, uint32_t lane,
-                                           uint64_t (&acc)[kSlots][Traits<F, N>::kOut]) {
-  if constexpr (F == Fmt::Q8) q8_chunk<N, C>(tile, xsb, lane, acc);
-  else twin_chunk<C>(tile, xsb, lane, acc);
+template <Fmt F, int N>
+__device__ __forceinline__ ChunkParams chunk_params(int c) {
+  if constexpr (F == Fmt::Q8) return q8_chunk_params(c);
+  else return twin_chunk_params(c);
 }
 
 template <Fmt F, int N>
-__device__ __forceinline__ void chunk_dispatch(int c, uint32_t tile, uint32_t xsb, uint32_t lane,
-                                               uint64_t (&acc)[kSlots][Traits<F, N>::kOut]) {
-#define PTI_CHUNK_CASE(C)                          \
-  case C:                                          \
-    chunk_body<F, N, C>(tile, xsb, lane, acc);     \
-    break;
-  switch (c) {
-    PTI_CHUNK_CASE(0) PTI_CHUNK_CASE(1) PTI_CHUNK_CASE(2) PTI_CHUNK_CASE(3) PTI_CHUNK_CASE(4)
-    PTI_CHUNK_CASE(5) PTI_CHUNK_CASE(6) PTI_CHUNK_CASE(7) PTI_CHUNK_CASE(8) PTI_CHUNK_CASE(9)
-    PTI_CHUNK_CASE(10) PTI_CHUNK_CASE(11) PTI_CHUNK_CASE(12) PTI_CHUNK_CASE(13)
-    case 14:
-      if constexpr (Traits<F, N>::kWarps > 14) chunk_body<F, N, 14>(tile, xsb, lane, acc);
-      break;
-    default: break;
-  }
-#undef PTI_CHUNK_CASE
-}
-
-// Stages the activations of super-blocks [wa, wb) as float2 column pairs.
-template <Fmt F, int N>
-__device__ __forceinline__ void stage_x(const GemvArgs &a, float *xs, int32_t wa, int32_t wb,
-                                        uint32_t tid) {
-  using T = Traits<F, N>;
-  constexpr int kConsumerThreads = T::kWarps * 32;
-  const int64_t k0 = static_cast<int64_t>(wa) * T::kColsPerSB;
-  const int32_t len = (wb - wa) * T::kColsPerSB;
+__device__ __forceinline__ void run_chunk(const ChunkParams &cp, const uint8_t *tile, const uint8_t *xsb,
+                                          uint32_t lane, uint32_t half,
+                                          uint64_t (&acc)[kTaskSlots][Traits<F, N>::kOut]) {
   if constexpr (F == Fmt::Q8) {
-    for (int32_t e = tid; e < N * len; e += kConsumerThreads) {
-      const int32_t s = e / len, kk = e - s * len;
-      xs[((kk >> 1) * T::kNS + s) * 2 + (kk & 1)] = a.x0[static_cast<int64_t>(s) * a.cols + k0 + kk];
+    switch (cp.cls) {
+      case -1: q8_body<N, -1>(tile, cp, xsb, lane, half, acc); break;
+      case 0: q8_body<N, 0>(tile, cp, xsb, lane, half, acc); break;
+      case 1: q8_body<N, 1>(tile, cp, xsb, lane, half, acc); break;
+      case 2: q8_body<N, 2>(tile, cp, xsb, lane, half, acc); break;
+      case 3: q8_body<N, 3>(tile, cp, xsb, lane, half, acc); break;
+      case 4: q8_body<N, 4>(tile, cp, xsb, lane, half, acc); break;
+      case 5: q8_body<N, 5>(tile, cp, xsb, lane, half, acc); break;
+      case 6: q8_body<N, 6>(tile, cp, xsb, lane, half, acc); break;
+      default: q8_body<N, 7>(tile, cp, xsb, lane, half, acc); break;
     }
   } else {
-    for (int32_t e = tid; e < 2 * len; e += kConsumerThreads) {
-      const int32_t s = e / len, kk = e - s * len;
-      const float *src = s ? a.x1 : a.x0;
-      xs[((kk >> 1) * 2 + s) * 2 + (kk & 1)] = src[k0 + kk];
+    switch (cp.cls) {
+      case -1: twin_body<N, -1>(tile, cp, xsb, lane, half, acc); break;
+      case 0: twin_body<N, 0>(tile, cp, xsb, lane, half, acc); break;
+      case 1: twin_body<N, 1>(tile, cp, xsb, lane, half, acc); break;
+      case 2: twin_body<N, 2>(tile, cp, xsb, lane, half, acc); break;
+      default: twin_body<N, 3>(tile, cp, xsb, lane, half, acc); break;
     }
   }
 }
@@ -353,10 +323,77 @@ __device__ __forceinline__ float tree_sum(float (&t)[K]) {
   return t[0];
 }
 
+// Sums the 8 warps' partials of one deferred row-tile segment (red slot `sl`)
+// and writes them: straight to y when no other CTA shares the tile, else as
+// this CTA's partial, the last CTA to finish the tile adding all partials in
+// CTA order.
+template <Fmt F, int N>
+__device__ __forceinline__ void finish_tile(const GemvArgs &a, const float *red, int sl, int32_t rb,
+                                            int32_t rb_first_cta, uint32_t tid, volatile uint32_t *flag) {
+  using T = Traits<F, N>;
+  constexpr int kOut = T::kOut;
+  constexpr int kConsumerThreads = T::kWarps * 32;
+  const int32_t c_lo = cta_of_unit(static_cast<int64_t>(rb) * a.n_sb, a.units, a.grid);
+  const int32_t c_hi = cta_of_unit(static_cast<int64_t>(rb + 1) * a.n_sb - 1, a.units, a.grid);
+  const bool shared_tile = c_hi > c_lo;
+  for (int t = tid; t < kOut * kRowsPerTile; t += kConsumerThreads) {
+    const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
+    const int h = row >> 6;
+    float v[T::kWarps / 2];
+#pragma unroll
+    for (int q = 0; q < T::kWarps / 2; ++q) {
+      const int w = (q >> 2) * 8 + h * 4 + (q & 3);  // the warps whose half is h
+      v[q] = red[((sl * T::kWarps + w) * kOut + s) * 64 + (row & 63)];
+    }
+    const float total = tree_sum(v);
+    const int64_t row_g = static_cast<int64_t>(rb) * kRowsPerTile + row;
+    if (!shared_tile) {
+      if (row_g < a.rows) {
+        if constexpr (F == Fmt::Q8) a.y0[s * a.rows + row_g] = total;
+        else (s == 0 ? a.y0 : a.y1)[row_g] = total;
+      }
+    } else {
+      a.part[((static_cast<int64_t>(blockIdx.x) * 2 + sl) * kOut + s) * kRowsPerTile + row] = total;
+    }
+  }
+  if (!shared_tile) return;
+  __threadfence();
+  named_barrier(kBarConsumers, kConsumerThreads);
+  if (tid == 0) {
+    const unsigned int prev = atomicAdd(&a.tickets[rb], 1u);
+    const bool last = prev == static_cast<unsigned int>(c_hi - c_lo);
+    if (last) {
+      a.tickets[rb] = 0u;  // leave the workspace zeroed for the next call
+      __threadfence();
+    }
+    flag[1] = last ? 1u : 0u;
+  }
+  named_barrier(kBarConsumers, kConsumerThreads);
+  if (flag[1] == 0) return;
+  for (int t = tid; t < kOut * kRowsPerTile; t += kConsumerThreads) {
+    const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
+    float total = 0.0f;
+    for (int32_t c = c_lo; c <= c_hi; ++c) {
+      const int cs = (rb == first_tile_of_cta(c, a.units, a.grid, a.n_sb)) ? 0 : 1;
+      float *const slot_ptr = &a.part[((static_cast<int64_t>(c) * 2 + cs) * kOut + s) * kRowsPerTile + row];
+      const float v = __ldcg(slot_ptr);
+      *slot_ptr = 0.0f;  // the whole workspace is zero again when the call completes
+      total = (c == c_lo) ? v : total + v;
+    }
+    const int64_t row_g = static_cast<int64_t>(rb) * kRowsPerTile + row;
+    if (row_g < a.rows) {
+      if constexpr (F == Fmt::Q8) a.y0[s * a.rows + row_g] = total;
+      else (s == 0 ? a.y0 : a.y1)[row_g] = total;
+    }
+  }
+  (void)rb_first_cta;
+}
+
 template <Fmt F, int N>
 __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
     gemv_tma_kernel(const __grid_constant__ CUtensorMap tmap, const GemvArgs a) {
   using T = Traits<F, N>;
+  using S = Stage<F, N>;
   constexpr int kOut = T::kOut;
   constexpr int kConsumerWarps = T::kWarps;
   constexpr int kConsumerThreads = kConsumerWarps * 32;
@@ -364,21 +401,20 @@ __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *const base_ptr = smem_raw + (base - raw);
-  const uint32_t xreg = base + kStages * kStageBytes;
-  float *const xs = reinterpret_cast<float *>(base_ptr + kStages * kStageBytes);
-  const uint32_t bars = xreg + a.x_region_bytes;
-  const uint32_t flags = bars + 2 * kStages * 8;
-  volatile uint32_t *const flag =
-      reinterpret_cast<volatile uint32_t *>(base_ptr + kStages * kStageBytes + a.x_region_bytes + 2 * kStages * 8);
+  const int stages = a.stages;
+  float *const red = reinterpret_cast<float *>(base_ptr + stages * S::kBytes);  // [2][warps][kOut][64]
+  const uint32_t bars = base + stages * S::kBytes + S::kRedBytes;             // full[stages], empty[stages]
+  const uint32_t flags = bars + 2 * stages * 8;
+  volatile uint32_t *const flag = reinterpret_cast<volatile uint32_t *>(base_ptr + (flags - base));
 
   const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t u0 = static_cast<int64_t>(blockIdx.x) * a.units / a.grid;
   const int64_t u1 = static_cast<int64_t>(blockIdx.x + 1) * a.units / a.grid;
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < stages; ++i) {
       mbar_init(bars + 8 * i, 1);
-      mbar_init(bars + 8 * (kStages + i), kConsumerWarps);
+      mbar_init(bars + 8 * (stages + i), kConsumerWarps);
     }
     flag[0] = 0;
     flag[1] = 0;
@@ -388,31 +424,69 @@ __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
   if (tid == 0) pdl_launch_dependents();
 
   if (warp == kConsumerWarps) {
-    // ---------------- producer: one lane issues every tile copy -------------
+    // ---------------- producer: one lane issues every copy --------------------
     if (lane == 0) {
       prefetch_tmap(&tmap);
       const uint64_t pol = l2_policy_evict_first();
       const int64_t nu = u1 - u0;
-      int64_t issued = 0;
-      for (int64_t i = 0; i < nu; ++i) {
-        const int stage = static_cast<int>(i % kStages);
-        const int64_t j = i / kStages;
-        if (j > 0 && !mbar_wait_bounded(bars + 8 * (kStages + stage), static_cast<uint32_t>((j - 1) & 1), flags)) {
+      const int64_t pre = nu < stages ? nu : stages;
+      auto unit_coords = [&](int64_t i, int32_t &rb, int32_t &sb) {
+        const int64_t u = u0 + i;
+        rb = static_cast<int32_t>(u / a.n_sb);
+        sb = static_cast<int32_t>(u - static_cast<int64_t>(rb) * a.n_sb);
+      };
+      auto load_x = [&](int64_t i, uint32_t slot) {
+        int32_t rb, sb;
+        unit_coords(i, rb, sb);
+        const uint32_t xdst = base + slot * S::kBytes + kStageBytes;
+        const uint32_t bar = bars + 8 * slot;
+        if constexpr (F == Fmt::Q8) {
+#pragma unroll
+          for (int st = 0; st < N; ++st)
+            bulk_load(xdst + st * S::kXStreamBytes, a.x0 + static_cast<int64_t>(st) * a.cols + static_cast<int64_t>(sb) * T::kColsPerSB,
+                      S::kXStreamBytes, bar);
+        } else {
+          bulk_load(xdst, a.x0 + static_cast<int64_t>(sb) * T::kColsPerSB, S::kXStreamBytes, bar);
+          bulk_load(xdst + S::kXStreamBytes, a.x1 + static_cast<int64_t>(sb) * T::kColsPerSB, S::kXStreamBytes, bar);
+        }
+      };
+      // Weights do not depend on the previous kernel in the stream: prefetch
+      // the first tiles before waiting for it, then fetch their activations.
+      for (int64_t i = 0; i < pre; ++i) {
+        int32_t rb, sb;
+        unit_coords(i, rb, sb);
+        mbar_expect_tx(bars + 8 * i, kStageBytes);
+        tma_load_2d(base + static_cast<uint32_t>(i) * S::kBytes, &tmap, 34 * sb, rb * kRowsPerTile, bars + 8 * i, pol);
+      }
+      pdl_wait_primary();
+      for (int64_t i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(bars + 8 * i, S::kXBytes);
+        load_x(i, static_cast<uint32_t>(i));
+      }
+      int64_t issued = pre;
+      uint32_t st = static_cast<uint32_t>(pre % stages), eph = 0;  // slot and empty-phase parity
+      for (int64_t i = pre; i < nu; ++i) {
+        const uint32_t empty = bars + 8 * (stages + st);
+        if (!mbar_try_wait(empty, eph) && !mbar_wait_bounded(empty, eph, flags)) {
           if (flag[0] == 0) atomicOr(&g_device_error, PTI_DEVERR_EMPTY_TIMEOUT);
           flag[0] = 1;
           break;
         }
         if (flag[0] != 0) break;
-        const int64_t u = u0 + i;
-        const int32_t rb = static_cast<int32_t>(u / a.n_sb);
-        const int32_t sb = static_cast<int32_t>(u - static_cast<int64_t>(rb) * a.n_sb);
-        mbar_arrive_expect_tx(bars + 8 * stage, kStageBytes);
-        tma_load_2d(base + stage * kStageBytes, &tmap, 34 * sb, rb * kRowsPerTile, bars + 8 * stage, pol);
+        int32_t rb, sb;
+        unit_coords(i, rb, sb);
+        mbar_arrive_expect_tx(bars + 8 * st, kStageBytes + S::kXBytes);
+        tma_load_2d(base + st * S::kBytes, &tmap, 34 * sb, rb * kRowsPerTile, bars + 8 * st, pol);
+        load_x(i, st);
         issued = i + 1;
+        if (++st == static_cast<uint32_t>(stages)) {
+          st = 0;
+          eph ^= 1u;
+        }
       }
       // Stay until every copy issued into this CTA's shared memory has landed.
-      for (int64_t i = (issued > kStages ? issued - kStages : 0); i < issued; ++i) {
-        if (!mbar_wait_bounded(bars + 8 * (i % kStages), static_cast<uint32_t>((i / kStages) & 1), 0))
+      for (int64_t i = (issued > stages ? issued - stages : 0); i < issued; ++i) {
+        if (!mbar_wait_bounded(bars + 8 * (i % stages), static_cast<uint32_t>((i / stages) & 1), 0))
           atomicOr(&g_device_error, PTI_DEVERR_DRAIN_TIMEOUT);
       }
     }
@@ -420,8 +494,19 @@ __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
   }
 
   // ---------------- consumers ----------------------------------------------
-  pdl_wait_primary();  // x may come from the previous kernel in the stream
-  uint64_t acc[kSlots][kOut];
+  uint64_t acc[kTaskSlots][kOut];
+  // Warp w runs on scheduler k = w % 4 (warps are dealt to the four schedulers
+  // round-robin) and always works on the same two chunks of every unit, rows
+  // of half j % 2 (j = w / 4): chunks k + 4(j/2) and k + 4(j/2) + 8, so each
+  // scheduler owns chunks k, k+4, k+8, k+12.  Chunk 16 of unit i goes to the
+  // warps j = 0, 1 of scheduler i % 4.
+  const uint32_t sched = warp & 3u, wj = warp >> 2;
+  const uint32_t half = wj & 1u;
+  const int ca = static_cast<int>(sched + 4u * (wj >> 1));
+  const ChunkParams pa = chunk_params<F, N>(ca), pb = chunk_params<F, N>(ca + 8),
+                    p16 = chunk_params<F, N>(16);
+  const bool takes16 = (wj >> 1) == 0u;
+  uint32_t st = 0, ph = 0;  // ring slot and phase parity of unit i
   int64_t i = 0;
   const int32_t rb_first = static_cast<int32_t>(u0 / a.n_sb);
   const int32_t rb_last = static_cast<int32_t>((u1 - 1) / a.n_sb);
@@ -429,105 +514,59 @@ __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
     const int32_t sb_begin = (rb == rb_first) ? static_cast<int32_t>(u0 - static_cast<int64_t>(rb) * a.n_sb) : 0;
     const int32_t sb_end = (rb == rb_last) ? static_cast<int32_t>(u1 - static_cast<int64_t>(rb) * a.n_sb) : a.n_sb;
 #pragma unroll
-    for (int r = 0; r < kSlots; ++r)
+    for (int r = 0; r < kTaskSlots; ++r)
 #pragma unroll
       for (int s = 0; s < kOut; ++s) acc[r][s] = 0ull;
 
-    for (int32_t wa = sb_begin; wa < sb_end; wa += a.xw_sb) {
-      const int32_t wb = min(sb_end, wa + a.xw_sb);
-      named_barrier(kBarConsumers, kConsumerThreads);  // x region free
-      stage_x<F, N>(a, xs, wa, wb, tid);
-      named_barrier(kBarConsumers, kConsumerThreads);
-      for (int32_t sb = wa; sb < wb; ++sb, ++i) {
-        const int stage = static_cast<int>(i % kStages);
-        bool ok = flag[0] == 0;
-        if (ok) ok = mbar_wait_bounded(bars + 8 * stage, static_cast<uint32_t>((i / kStages) & 1), flags);
+    for (int32_t sb = sb_begin; sb < sb_end; ++sb, ++i) {
+      const uint32_t full = bars + 8 * st;
+      bool ok = mbar_try_wait(full, ph);
+      if (!ok) {
+        ok = flag[0] == 0 && mbar_wait_bounded(full, ph, flags);
         if (!ok && flag[0] == 0) {
           atomicOr(&g_device_error, PTI_DEVERR_FULL_TIMEOUT);
           flag[0] = 1;
         }
-        if (ok) {
-          const uint32_t tile = base + stage * kStageBytes;
-          const uint32_t xsb = xreg + (sb - wa) * T::kXBytesPerSB;
-          // warp w owns chunk w; the 17 - kConsumerWarps remaining chunks rotate
-          chunk_dispatch<F, N>(static_cast<int>(warp), tile, xsb, lane, acc);
-          constexpr int kExtra = 17 - kConsumerWarps;
-          const int64_t e0 = static_cast<int64_t>(kExtra) * i;
-          if constexpr (kExtra == 3) {
-            if (warp == static_cast<uint32_t>(e0 % kConsumerWarps)) chunk_body<F, N, 14>(tile, xsb, lane, acc);
-          }
-          if (warp == static_cast<uint32_t>((e0 + kExtra - 2) % kConsumerWarps))
-            chunk_body<F, N, 15>(tile, xsb, lane, acc);
-          if (warp == static_cast<uint32_t>((e0 + kExtra - 1) % kConsumerWarps))
-            chunk_body<F, N, 16>(tile, xsb, lane, acc);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars + 8 * (kStages + stage));
+      }
+      if (ok) {
+        const uint8_t *tile = base_ptr + st * S::kBytes;
+        const uint8_t *xsb = tile + kStageBytes;
+        run_chunk<F, N>(pa, tile, xsb, lane, half, acc);
+        run_chunk<F, N>(pb, tile, xsb, lane, half, acc);
+        if (takes16 && (static_cast<uint32_t>(i) & 3u) == sched) run_chunk<F, N>(p16, tile, xsb, lane, half, acc);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8 * (stages + st));
+      if (++st == static_cast<uint32_t>(stages)) {
+        st = 0;
+        ph ^= 1u;
       }
     }
 
-    // ---- reduce the 15 warps' partial sums of this row tile (fixed order) ----
-    named_barrier(kBarConsumers, kConsumerThreads);  // every warp is done with x
-    float *const red = xs;                            // [warp][kOut][128]
+    // ---- park this warp's sums for the tile: slot 0 = first tile of the CTA,
+    //      slot 1 = any later one (only the last can be shared with another CTA)
+    const int sl = (rb == rb_first) ? 0 : 1;
+    const bool middle = rb != rb_first && rb != rb_last;
 #pragma unroll
-    for (int r = 0; r < kSlots; ++r)
+    for (int r = 0; r < kTaskSlots; ++r)
 #pragma unroll
       for (int s = 0; s < kOut; ++s) {
         const float2 v = unpack2(acc[r][s]);
-        red[(warp * kOut + s) * kRowsPerTile + r * 32 + lane] = v.x + v.y;
+        red[((sl * kConsumerWarps + warp) * kOut + s) * 64 + r * 32 + lane] = v.x + v.y;
       }
+    if (middle) {
+      // a tile wholly inside this CTA's range: finish it now (rare: only when
+      // a CTA spans more than two row tiles)
+      named_barrier(kBarConsumers, kConsumerThreads);
+      finish_tile<F, N>(a, red, 1, rb, rb_first, tid, flag);
+      named_barrier(kBarConsumers, kConsumerThreads);
+    }
+  }
+  named_barrier(kBarConsumers, kConsumerThreads);
+  finish_tile<F, N>(a, red, 0, rb_first, rb_first, tid, flag);
+  if (rb_last != rb_first) {
     named_barrier(kBarConsumers, kConsumerThreads);
-
-    const int32_t c_lo = cta_of_unit(static_cast<int64_t>(rb) * a.n_sb, a.units, a.grid);
-    const int32_t c_hi = cta_of_unit(static_cast<int64_t>(rb + 1) * a.n_sb - 1, a.units, a.grid);
-    const bool shared_tile = c_hi > c_lo;
-    const int slot = (rb == rb_first) ? 0 : 1;
-    for (int t = tid; t < kOut * kRowsPerTile; t += kConsumerThreads) {
-      const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
-      float v[kConsumerWarps];
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) v[w] = red[(w * kOut + s) * kRowsPerTile + row];
-      const float total = tree_sum(v);
-      const int64_t row_g = static_cast<int64_t>(rb) * kRowsPerTile + row;
-      if (!shared_tile) {
-        if (row_g < a.rows) {
-          if constexpr (F == Fmt::Q8) a.y0[s * a.rows + row_g] = total;
-          else (s == 0 ? a.y0 : a.y1)[row_g] = total;
-        }
-      } else {
-        a.part[((static_cast<int64_t>(blockIdx.x) * 2 + slot) * kOut + s) * kRowsPerTile + row] = total;
-      }
-    }
-    if (shared_tile) {
-      __threadfence();
-      named_barrier(kBarConsumers, kConsumerThreads);
-      if (tid == 0) {
-        const unsigned int prev = atomicAdd(&a.tickets[rb], 1u);
-        const bool last = prev == static_cast<unsigned int>(c_hi - c_lo);
-        if (last) {
-          a.tickets[rb] = 0u;  // leave the workspace zeroed for the next call
-          __threadfence();
-        }
-        flag[1] = last ? 1u : 0u;
-      }
-      named_barrier(kBarConsumers, kConsumerThreads);
-      if (flag[1] != 0) {
-        for (int t = tid; t < kOut * kRowsPerTile; t += kConsumerThreads) {
-          const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
-          float total = 0.0f;
-          for (int32_t c = c_lo; c <= c_hi; ++c) {
-            const int sl = (rb == first_tile_of_cta(c, a.units, a.grid, a.n_sb)) ? 0 : 1;
-            const float v = __ldcg(&a.part[((static_cast<int64_t>(c) * 2 + sl) * kOut + s) * kRowsPerTile + row]);
-            total = (c == c_lo) ? v : total + v;
-          }
-          const int64_t row_g = static_cast<int64_t>(rb) * kRowsPerTile + row;
-          if (row_g < a.rows) {
-            if constexpr (F == Fmt::Q8) a.y0[s * a.rows + row_g] = total;
-            else (s == 0 ? a.y0 : a.y1)[row_g] = total;
-          }
-        }
-      }
-    }
+    finish_tile<F, N>(a, red, 1, rb_last, rb_first, tid, flag);
   }
 }
 
@@ -626,26 +665,22 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 struct TilePlan {
   int64_t n_sb = 0, n_rb = 0, units = 0;
-  int32_t grid = 0, xw_sb = 0;
-  uint32_t x_region = 0;
+  int32_t grid = 0, stages = 0;
   size_t smem = 0;
 };
 
 template <Fmt F, int N>
 TilePlan plan_tiles(int64_t rows, int64_t cols, int sms) {
   using T = Traits<F, N>;
+  using S = Stage<F, N>;
   TilePlan p;
   p.n_sb = cols / T::kColsPerSB;
   p.n_rb = (rows + kRowsPerTile - 1) / kRowsPerTile;
   p.units = p.n_sb * p.n_rb;
   p.grid = static_cast<int32_t>(std::min<int64_t>({static_cast<int64_t>(sms), p.units, kMaxGrid}));
-  const int64_t per_cta = (p.units + p.grid - 1) / p.grid;
-  const int64_t red_bytes = static_cast<int64_t>(T::kWarps) * T::kOut * kRowsPerTile * 4;
-  const int64_t avail = kSmemOptin - 1024 - static_cast<int64_t>(kStages) * kStageBytes - kBarBytes;
-  p.xw_sb = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(per_cta, avail / T::kXBytesPerSB)));
-  p.x_region = static_cast<uint32_t>(std::max<int64_t>(static_cast<int64_t>(p.xw_sb) * T::kXBytesPerSB, red_bytes));
-  p.x_region = (p.x_region + 15u) & ~15u;
-  p.smem = 1024 + static_cast<size_t>(kStages) * kStageBytes + p.x_region + kBarBytes;
+  const int64_t fixed = 1024 + S::kRedBytes + 16 * kMaxStages + 16;
+  p.stages = static_cast<int32_t>(std::min<int64_t>(kMaxStages, (kSmemOptin - fixed) / S::kBytes));
+  p.smem = static_cast<size_t>(fixed) + static_cast<size_t>(p.stages) * S::kBytes;
   return p;
 }
 
@@ -659,13 +694,13 @@ size_t fast_workspace_bytes(int64_t rows, int kout) {
 
 template <Fmt F, int N>
 pti_status launch_fast(const void *w, int64_t rows, int64_t cols, const float *x0, const float *x1,
-                       float *y0, float *y1, void *workspace, cudaStream_t stream) {
+                       float *y0, float *y1, void *workspace, cudaStream_t stream, bool pdl = false) {
   using T = Traits<F, N>;
   int dev = 0;
   const int sms = current_device_sms(&dev);
   if (sms <= 0) return PTI_ERR_CUDA;
   const TilePlan p = plan_tiles<F, N>(rows, cols, sms);
-  if (p.smem > static_cast<size_t>(kSmemOptin)) return PTI_ERR_SHAPE;
+  if (p.stages < 2 || p.smem > static_cast<size_t>(kSmemOptin)) return PTI_ERR_SHAPE;
 
   static std::mutex mu;
   static bool attr_done[128] = {};
@@ -707,9 +742,18 @@ pti_status launch_fast(const void *w, int64_t rows, int64_t cols, const float *x
   a.n_sb = static_cast<int32_t>(p.n_sb);
   a.n_rb = static_cast<int32_t>(p.n_rb);
   a.grid = p.grid;
-  a.xw_sb = p.xw_sb;
-  a.x_region_bytes = p.x_region;
-  gemv_tma_kernel<F, N><<<p.grid, T::kWarps * 32 + 32, p.smem, stream>>>(tmap, a);
+  a.stages = p.stages;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+  cfg.blockDim = dim3(T::kWarps * 32 + 32);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, gemv_tma_kernel<F, N>, tmap, a) != cudaSuccess) return launch_status();
   return launch_status();
 }
 
@@ -782,7 +826,7 @@ extern "C" pti_status pti_q8_gemv_nstream(const void *w_q8, int64_t rows, int64_
       return PTI_ERR_ALIAS;
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (need > 0) {
+  if (need > 0 && aligned(x, 16)) {
     switch (n_streams) {
       case 1: return launch_fast<Fmt::Q8, 1>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st);
       case 2: return launch_fast<Fmt::Q8, 2>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st);
@@ -823,7 +867,8 @@ extern "C" pti_status pti_ssq_twin_gemv(const void *w_twin, int64_t rows, int64_
         overlaps(workspace, need, x_b, x_bytes) || overlaps(workspace, need, y_a, y_bytes) ||
         overlaps(workspace, need, y_b, y_bytes))
       return PTI_ERR_ALIAS;
-    return launch_fast<Fmt::Twin, 2>(w_twin, rows, cols, x_a, x_b, y_a, y_b, workspace, st);
+    if (aligned(x_a, 16) && aligned(x_b, 16))
+      return launch_fast<Fmt::Twin, 2>(w_twin, rows, cols, x_a, x_b, y_a, y_b, workspace, st);
   }
   const int sms = current_device_sms();
   if (sms <= 0) return PTI_ERR_CUDA;

@@ -126,6 +126,7 @@ extern "C" pti_status pti_verify_greedy(const float *logits, const int32_t *gues
   if (n_streams < 1 || n_streams > 4) return PTI_ERR_NSTREAMS;
   if (steps < 0 || vocab < 1 || vocab > INT_MAX) return PTI_ERR_SHAPE;
   if (steps > (int64_t{1} << 40) / (static_cast<int64_t>(n_streams) * vocab)) return PTI_ERR_SHAPE;
+  if (steps == 0) return PTI_OK;  // nothing is read or written: pointers may be NULL
   if (logits == nullptr || guess == nullptr || argmax_out == nullptr || accept_len_out == nullptr ||
       (n_streams > 1 && match_out == nullptr))
     return PTI_ERR_NULL;
@@ -144,7 +145,6 @@ extern "C" pti_status pti_verify_greedy(const float *logits, const int32_t *gues
     for (int j = i + 1; j < 3; ++j)
       if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return PTI_ERR_ALIAS;
   }
-  if (steps == 0) return PTI_OK;
   const int sms = current_device_sms();
   if (sms <= 0) return PTI_ERR_CUDA;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(steps, static_cast<int64_t>(sms) * 4));

@@ -248,3 +248,41 @@ def test_workspace_reuse_across_calls():
         y = pti.q8_gemv_nstream(w, rows, cols, dev(x), ws=ws).cpu().numpy()
         y_ref, bound = oracle.q8_gemv(w_np, rows, cols, x)
         assert_parity(y, y_ref, bound, f"call {k}")
+
+
+def test_one_workspace_serves_every_shape_and_stream_count():
+    """One zero-filled workspace shared, in turn, by Q8 calls of different shapes
+    and stream counts and by twin calls: every call matches the oracle (each call
+    must leave the whole workspace zero-filled for the next one)."""
+    ws = torch.zeros(pti.q8_gemv_workspace_bytes(5120, 17408, 4), dtype=torch.uint8, device="cuda")
+    cases = [("q8", 1000, 2048, 4), ("q8", 520, 1024, 1), ("twin", 520, 1024, 2), ("q8", 1000, 2048, 2),
+             ("twin", 1000, 2048, 2), ("q8", 520, 1024, 3), ("q8", 1000, 2048, 1)]
+    for k, (kind, rows, cols, n) in enumerate(cases):
+        if kind == "q8":
+            w = pti_synth.q8_matrix(rows, cols, seed=40 + k)
+            x = pti_synth.activations(n, cols, seed=40 + k)
+            y = pti.q8_gemv_nstream(dev(w), rows, cols, dev(x), ws=ws).cpu().numpy()
+            y_ref, bound = oracle.q8_gemv(w, rows, cols, x)
+            assert_parity(y, y_ref, bound, f"case {k}")
+        else:
+            w = pti_synth.twin_matrix(rows, cols, seed=40 + k)
+            xa, xb = pti_synth.activations(2, cols, seed=40 + k)
+            ya, yb = pti.ssq_twin_gemv(dev(w), rows, cols, dev(xa), dev(xb), ws=ws)
+            ra, rb, ba, bb = oracle.twin_gemv(w, rows, cols, xa, xb)
+            assert_parity(ya.cpu().numpy(), ra, ba, f"case {k} A")
+            assert_parity(yb.cpu().numpy(), rb, bb, f"case {k} B")
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero()) == 0
+
+
+def test_unaligned_activations_take_the_plain_path():
+    """x offset by 4 bytes (not 16-byte aligned): still correct."""
+    rows, cols = 300, 1024
+    w = pti_synth.q8_matrix(rows, cols, seed=77)
+    x = pti_synth.activations(2, cols, seed=77)
+    buf = torch.empty(2 * cols + 1, dtype=torch.float32, device="cuda")
+    xv = buf[1:].view(2, cols)
+    xv.copy_(dev(x))
+    y = pti.q8_gemv_nstream(dev(w), rows, cols, xv).cpu().numpy()
+    y_ref, bound = oracle.q8_gemv(w, rows, cols, x)
+    assert_parity(y, y_ref, bound, "unaligned x")
