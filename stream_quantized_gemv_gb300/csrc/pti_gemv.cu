@@ -55,6 +55,7 @@ namespace {
 constexpr int kSBBytes = 272;                          // super-block bytes (17 chunks of 16)
 constexpr int kRowsPerTile = 128;                      // rows per unit
 constexpr int kMaxStages = 6;
+constexpr int kWarpCount = 16;  // consumer warps, 4 per scheduler
 constexpr int kStageBytes = kRowsPerTile * kSBBytes;   // 34816
 constexpr int kMaxGrid = 320;
 constexpr int kSmemOptin = 232448;                     // 227 KB per CTA
@@ -69,7 +70,7 @@ struct Traits;
 template <int N>
 struct Traits<Fmt::Q8, N> {
   static constexpr int kOut = N;                   // output vectors
-  static constexpr int kWarps = 16;   // consumer warps (4 per scheduler)
+  static constexpr int kWarps = kWarpCount;
   static constexpr int kColsPerSB = 256;
   static constexpr int kXStreams = N;
   static constexpr int kBlockBytes = 34;
@@ -77,7 +78,7 @@ struct Traits<Fmt::Q8, N> {
 template <int N>
 struct Traits<Fmt::Twin, N> {
   static constexpr int kOut = 2;
-  static constexpr int kWarps = 16;
+  static constexpr int kWarps = kWarpCount;
   static constexpr int kColsPerSB = 128;
   static constexpr int kXStreams = 2;
   static constexpr int kBlockBytes = 68;
@@ -105,7 +106,8 @@ struct GemvArgs {
 };
 
 // Rows handled by one warp task: lane l owns rows 64h + l and 64h + 32 + l of
-// the tile (h = the task's half).
+// the tile (h = the task's half).  (Four rows per lane halves the activation
+// loads per weight but doubles the code of each chunk body; measured slower.)
 constexpr int kTaskSlots = 2;
 
 // Where a 16-byte chunk's weights sit.  Chunks come in a few structural
@@ -338,11 +340,10 @@ __device__ __forceinline__ void finish_tile(const GemvArgs &a, const float *red,
   const bool shared_tile = c_hi > c_lo;
   for (int t = tid; t < kOut * kRowsPerTile; t += kConsumerThreads) {
     const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
-    const int h = row >> 6;
     float v[T::kWarps / 2];
 #pragma unroll
     for (int q = 0; q < T::kWarps / 2; ++q) {
-      const int w = (q >> 2) * 8 + h * 4 + (q & 3);  // the warps whose half is h
+      const int w = (q >> 2) * 8 + (row >> 6) * 4 + (q & 3);  // the warps whose half is row / 64
       v[q] = red[((sl * T::kWarps + w) * kOut + s) * 64 + (row & 63)];
     }
     const float total = tree_sum(v);
