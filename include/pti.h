@@ -103,6 +103,32 @@ pti_status pti_q8_gemv_nstream(const void *w_q8, int64_t rows, int64_t cols, int
                                pti_stream_t stream);
 
 /*
+ * Allocation-free N-stream Q8 GEMV.  The pages have no counterpart: this is a
+ * library convenience for callers that cannot allocate device memory, such as
+ * a plug-in running inside a host runtime that owns every device allocation
+ * through its own pool, or a decode loop that must not call the CUDA allocator
+ * once it runs (freeing device memory synchronises the whole device).
+ *
+ * Same arguments, results and checks as pti_q8_gemv_nstream, without the
+ * workspace: the scratch it needs lives in a 2 MiB array inside this library
+ * (pti_q8_gemv_noalloc_max_scratch_bytes()), held by every GPU that loads the
+ * library until the process exits.  It serves any shape whose workspace fits,
+ * i.e. up to 25,165,824 rows at n_streams = 4 (56,623,104 at n_streams = 1) on
+ * the cols % 256 == 0 path; larger requests return PTI_ERR_WORKSPACE before
+ * anything is enqueued.  The call allocates nothing.
+ *
+ * The first call on a device sets the array up (looks up its device address,
+ * zero-fills it and synchronises the device); make that first call before any
+ * stream capture.  All calls on a device share the one array, which keeps the
+ * last call's contents (every completed call leaves it zero-filled): calls
+ * that overlap on the GPU race, so order them (one stream, or synchronise).
+ */
+size_t pti_q8_gemv_noalloc_max_scratch_bytes(void);
+
+pti_status pti_q8_gemv_nstream_noalloc(const void *w_q8, int64_t rows, int64_t cols, int n_streams,
+                                       const float *x, float *y, pti_stream_t stream);
+
+/*
  * SSQ mode-16 twin GEMV.
  *   [PTI-readme] §"与 SSQ（Side-by-Side Quantization）的关系": per uint16 pw,
  *   wa = (int8)(pw >> 8), wb = (int8)(pw & 0xFF); acc_a += scale_a*wa*x_a[i],

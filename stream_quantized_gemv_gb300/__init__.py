@@ -69,6 +69,10 @@ def lib() -> ctypes.CDLL:
             L.pti_ssq_twin_gemv.argtypes = [P, I64, I64, P, P, P, P, P, SZ, P]
             L.pti_verify_greedy.restype = I
             L.pti_verify_greedy.argtypes = [P, P, I64, I, I64, P, P, P, P]
+            L.pti_q8_gemv_noalloc_max_scratch_bytes.restype = SZ
+            L.pti_q8_gemv_noalloc_max_scratch_bytes.argtypes = []
+            L.pti_q8_gemv_nstream_noalloc.restype = I
+            L.pti_q8_gemv_nstream_noalloc.argtypes = [P, I64, I64, I, P, P, P]
             L.pti_device_error.restype = I
             L.pti_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             _lib = L
@@ -165,6 +169,20 @@ def verify_greedy(logits, guess, argmax=None, match=None, accept=None, stream=No
     _check(lib().pti_verify_greedy(_ptr(logits), _ptr(guess), steps, n, vocab, _ptr(argmax), match_ptr,
                                    _ptr(accept), _stream(stream)), "pti_verify_greedy")
     return argmax, match, accept
+
+
+def q8_gemv_nstream_noalloc(w, rows: int, cols: int, x, y=None, stream=None):
+    """As ``q8_gemv_nstream`` but with the library's built-in scratch instead of
+    a workspace (for callers that cannot allocate device memory)."""
+    import torch
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    n = x.shape[0]
+    if y is None:
+        y = torch.empty((n, rows), dtype=torch.float32, device=x.device)
+    _check(lib().pti_q8_gemv_nstream_noalloc(_ptr(w), rows, cols, n, _ptr(x), _ptr(y), _stream(stream)),
+           "pti_q8_gemv_nstream_noalloc")
+    return y
 
 
 def device_error() -> int:

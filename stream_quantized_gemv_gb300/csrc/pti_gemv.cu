@@ -879,6 +879,62 @@ extern "C" pti_status pti_ssq_twin_gemv(const void *w_twin, int64_t rows, int64_
   return launch_status();
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the N-stream Q8 GEMV.
+//
+// Some callers cannot allocate device memory for the workspace: a plug-in that
+// runs inside another runtime which owns every device allocation through its
+// own memory pool and only hands out input and output buffers, or a decode
+// loop that must not call into the CUDA allocator once it is running (freeing
+// device memory synchronises the whole device and stalls every stream).  For
+// them the workspace lives in this file-scope array, reserved when the library
+// is loaded and kept by every GPU that loads it until the process exits.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = size_t{2} << 20;  // 2 MiB per device
+static __device__ __align__(256) unsigned char g_pti_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+// Device address of g_pti_noalloc_scratch on the current device.  The first
+// call on a device looks the address up (the array's name is only a host-side
+// stand-in), zero-fills the array and synchronises the device.
+pti_status noalloc_scratch_address(void **out) {
+  static std::mutex mu;
+  static void *addr[128] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) {
+    cudaGetLastError();
+    return PTI_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pti_noalloc_scratch) != cudaSuccess || p == nullptr) return launch_status();
+    if (cudaMemset(p, 0, kNoAllocScratchBytes) != cudaSuccess) return launch_status();
+    if (cudaDeviceSynchronize() != cudaSuccess) return launch_status();
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return PTI_OK;
+}
+}  // namespace
+
+extern "C" size_t pti_q8_gemv_noalloc_max_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" pti_status pti_q8_gemv_nstream_noalloc(const void *w_q8, int64_t rows, int64_t cols, int n_streams,
+                                                  const float *x, float *y, pti_stream_t stream) {
+  if (w_q8 == nullptr || x == nullptr || y == nullptr) return PTI_ERR_NULL;
+  if (const pti_status st = check_gemv_shape(rows, cols); st != PTI_OK) return st;
+  if (n_streams < 1 || n_streams > 4) return PTI_ERR_NSTREAMS;
+  const size_t need = pti_q8_gemv_workspace_bytes(rows, cols, n_streams);
+  if (need > kNoAllocScratchBytes) return PTI_ERR_WORKSPACE;  // more rows than the built-in scratch serves
+  void *scratch = nullptr;
+  if (need > 0) {
+    if (const pti_status st = noalloc_scratch_address(&scratch); st != PTI_OK) return st;
+  }
+  return pti_q8_gemv_nstream(w_q8, rows, cols, n_streams, x, y, scratch, need > 0 ? kNoAllocScratchBytes : 0,
+                             stream);
+}
+
 extern "C" pti_status pti_device_error(uint32_t *code_out) {
   if (code_out == nullptr) return PTI_ERR_NULL;
   if (cudaDeviceSynchronize() != cudaSuccess) return launch_status();
