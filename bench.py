@@ -1,8 +1,11 @@
 """Benchmark of the Packed Twin Inference hot path on GB300.
 
-Default line (N=1 GPU): the multi-stream Q8 weight pass, N = 4 activation
-streams through Qwen3.6-27B-shaped Q8 matrices (FFN 17408 x hidden 5120), one
-step = one pass over L distinct matrices (each weight read once per step).
+Default line (N=1 GPU): the 4-stream decode weight pass, 64 layers of Q8 gate
+and up (17408 x 5120) and down (5120 x 17408) GEMVs with the SiLU and RMS
+glue, N = 4 fp32 activation streams chained layer to layer; one step = one
+pass over all 18.2 GB of distinct weights (each byte read once per step).
+Other lines: ``--workload q8`` (the N-stream Q8 GEMV over distinct
+17408 x 5120 matrices), ``twin``, ``verify``, ``all``.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -306,7 +309,67 @@ class VerifyBatch(Q8Pass):
         return run, b, f"oracle verify_greedy on {steps} of the {self.steps} steps"
 
 
+class DecodePass(Q8Pass):
+    """The chained decode weight pass: L layers of gate/up/down Q8 GEMVs with
+    the fused SiLU and RMS glue, N streams (one step = one pass)."""
+
+    def __init__(self, hidden=5120, ffn=17408, n=4, layers=64, seed=0):
+        import torch
+        import pti_synth
+        import stream_quantized_gemv_gb300 as pti
+        self.pti, self.torch = pti, torch
+        self.hidden, self.ffn, self.n, self.layers = hidden, ffn, n, layers
+        self.name = f"mlp_decode_pass_n{n}_{hidden}x{ffn}_x{layers}"
+        gate = [pti_synth.q8_matrix_device(ffn, hidden, seed, 3 * l) for l in range(layers)]
+        up = [pti_synth.q8_matrix_device(ffn, hidden, seed, 3 * l + 1) for l in range(layers)]
+        down = [pti_synth.q8_matrix_device(hidden, ffn, seed, 3 * l + 2) for l in range(layers)]
+        self.weights = pti.DecodeWeights(gate, up, down)
+        self.x = pti_synth.activations_device(n, hidden, seed, 1000)
+        self.y = torch.empty((n, hidden), dtype=torch.float32, device="cuda")
+        need = pti.mlp_decode_pass_workspace_bytes(hidden, ffn, n)
+        self.ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+        self.weight_bytes = 3 * ffn * (hidden // 32) * Q8_BLOCK   # per layer
+        # algorithmic bytes: every weight once, each kernel's input and output vectors once
+        act = 4 * n * ((hidden + ffn) + (ffn + hidden))
+        self.step_bytes = layers * (self.weight_bytes + act) + 4 * n * 2 * hidden
+        self.launch_bytes = self.step_bytes / (2 * layers)       # mean over the pass's GEMV launches
+        self.launches_per_step = 2 * layers + 1
+        self.gemv_launches_per_step = 2 * layers
+        self.tokens_per_step = n
+        self.dominant = f"gemv_tma_kernel<Q8,{n},GateUp|Down> (the pass's {2 * layers} GEMV launches)"
+        self.dtype = "f32"
+
+    def step(self, x=None, y=None):
+        x = self.x if x is None else x
+        y = self.y if y is None else y
+        self.pti.mlp_decode_pass(self.weights, self.hidden, self.ffn, x, x_out=y, ws=self.ws)
+
+    def config(self):
+        return {"workload": f"{self.layers}-layer decode weight pass, N={self.n} fp32 streams: per layer Q8 gate "
+                            f"and up {self.ffn}x{self.hidden}, SiLU(g)*u, RMS, Q8 down {self.hidden}x{self.ffn}, "
+                            "RMS; distinct random weights per layer",
+                "hidden": self.hidden, "ffn": self.ffn, "n_streams": self.n, "layers": self.layers,
+                "weight_bytes_per_step": self.layers * self.weight_bytes,
+                "l2": f"inputs larger than L2: {self.layers * self.weight_bytes / 1e9:.2f} GB of distinct "
+                      "weights per step, streamed with an L2 evict-first policy"}
+
+    def cpu_sample(self):
+        import oracle
+        import pti_synth
+        hidden, ffn = 1024, 3584     # one layer of the same structure at a fifth of the width
+        wg = pti_synth.q8_matrix(ffn, hidden, seed=0, tensor_id=0)
+        wu = pti_synth.q8_matrix(ffn, hidden, seed=0, tensor_id=1)
+        wd = pti_synth.q8_matrix(hidden, ffn, seed=0, tensor_id=2)
+        x = pti_synth.activations(self.n, hidden, seed=0, tensor_id=1000)
+        b = 3 * ffn * (hidden // 32) * Q8_BLOCK + 4 * self.n * 2 * (hidden + ffn)
+
+        def run():
+            oracle.mlp_layer(wg, wu, wd, hidden, ffn, x)
+        return run, b, f"oracle mlp_layer: one {hidden}x{ffn} layer (gate, up, down), N={self.n}"
+
+
 WORKLOADS = {
+    "decode": lambda a: DecodePass(a.cols or 5120, a.rows or 17408, a.n, a.layers or 64),
     "q8": lambda a: Q8Pass(a.rows or 17408, a.cols or 5120, a.n, a.layers or 16),
     "twin": lambda a: TwinPass(a.rows or 17408, a.cols or 5120, a.layers or 8),
     "verify": lambda a: VerifyBatch(),
@@ -402,7 +465,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="q8", choices=sorted(WORKLOADS) + ["all"])
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS) + ["all"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--n", type=int, default=4)
     ap.add_argument("--rows", type=int, default=0)
@@ -453,7 +516,7 @@ def main():
         e2e_ms, h2d, d2h = time_e2e(wl, max(3, a.steps // 2), 2)
         err = pti.device_error()
         value = wl.step_bytes * world / (ms * 1e-3) / 1e9
-        per_launch_ms = ms / wl.launches_per_step
+        per_launch_ms = ms / getattr(wl, "gemv_launches_per_step", wl.launches_per_step)
         achieved = wl.launch_bytes / (per_launch_ms * 1e-3) / 1e9
         traffic = recorded_traffic(wl.name)
         line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -494,9 +557,12 @@ class _CpuOnly:
 
 def _cpu_only_workload(name, a):
     """The workload's config and CPU sample without allocating device memory."""
-    cls = {"q8": Q8Pass, "twin": TwinPass, "verify": VerifyBatch}[name]
+    cls = {"decode": DecodePass, "q8": Q8Pass, "twin": TwinPass, "verify": VerifyBatch}[name]
     wl = cls.__new__(cls)
-    if name == "q8":
+    if name == "decode":
+        wl.hidden, wl.ffn, wl.n, wl.layers = a.cols or 5120, a.rows or 17408, a.n, a.layers or 64
+        wl.weight_bytes = 3 * wl.ffn * (wl.hidden // 32) * Q8_BLOCK
+    elif name == "q8":
         wl.rows, wl.cols, wl.n, wl.layers = a.rows or 17408, a.cols or 5120, a.n, a.layers or 16
         wl.weight_bytes = wl.rows * (wl.cols // 32) * Q8_BLOCK
     elif name == "twin":

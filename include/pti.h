@@ -10,6 +10,9 @@
  *                         matrix computes y_A = W_A x_A and y_B = W_B x_B.
  *   pti_verify_greedy     greedy verify: per-stream argmax, guess == actual and
  *                         the accepted-prefix length of every step.
+ *   pti_mlp_decode_pass   a chained decode pass: n_layers gated-MLP layers
+ *                         (gate, up, SiLU, RMS, down, RMS) over 1..4 streams,
+ *                         one pass over the weights for all streams.
  *
  * Sources are cited by page title and section:
  *   [PTI-forum]  "Packed Twin Inference：无需草稿模型的推测解码新方案，实现2倍吞吐量提升"
@@ -61,12 +64,13 @@ typedef struct CUstream_st *pti_stream_t; /* identical to cudaStream_t */
 typedef enum pti_status {
     PTI_OK = 0,
     PTI_ERR_NULL = 1,      /* a required pointer is NULL */
-    PTI_ERR_SHAPE = 2,     /* rows < 1, cols < 32, cols % 32 != 0, steps < 0, vocab < 1, too large */
-    PTI_ERR_NSTREAMS = 3,  /* n_streams outside [1, 4] (layers < 1 for the decode pass) */
+    PTI_ERR_SHAPE = 2,     /* rows < 1, cols < 32, cols % 32 != 0, steps < 0, vocab < 1, layers < 1, too large */
+    PTI_ERR_NSTREAMS = 3,  /* n_streams outside [1, 4] */
     PTI_ERR_ALIGN = 4,     /* a pointer is not aligned as documented */
     PTI_ERR_ALIAS = 5,     /* an output overlaps an input or another output */
     PTI_ERR_CUDA = 6,      /* the CUDA runtime reported an error (no device, launch failure) */
-    PTI_ERR_WORKSPACE = 7  /* workspace missing or smaller than required */
+    PTI_ERR_WORKSPACE = 7, /* workspace missing or smaller than required */
+    PTI_ERR_VALUE = 8      /* a scalar argument outside its documented range (eps) */
 } pti_status;
 
 /* Human-readable name of a status code (static storage, never NULL). */
@@ -173,6 +177,58 @@ pti_status pti_verify_greedy(const float *logits, const int32_t *guess,
                              int64_t steps, int n_streams, int64_t vocab,
                              int32_t *argmax_out, uint8_t *match_out, int32_t *accept_len_out,
                              pti_stream_t stream);
+
+/*
+ * Chained decode pass over n_layers gated-MLP layers.
+ *   A decode step of the N streams is one pass over all the weights for all N
+ *   streams ([PTI-readme] §"带宽分析：为什么会有开销"; [PTI-forum] §"技术实现架构",
+ *   step 2).  The layer is the gated MLP (W_gate, W_up, W_down) of [CS336-L10]
+ *   §"2.4 MLP 层的算术强度"; the pages name no nonlinearity or normalisation,
+ *   so this library takes SiLU and an RMS rescale after h and after the layer:
+ *     g = W_gate x,  u = W_up x                 (ffn rows, hidden columns)
+ *     h = rms(SiLU(g) * u)                      rms(v) = v / sqrt(mean(v^2) + eps)
+ *     x <- rms(W_down h)                        (hidden rows, ffn columns)
+ *   for every stream s independently.
+ *
+ *   w_gate, w_up, w_down  HOST arrays of n_layers DEVICE pointers: layer l
+ *              reads w_gate[l] and w_up[l] ([ffn][hidden/32] Q8 blocks) and
+ *              w_down[l] ([hidden][ffn/32] Q8 blocks), each 16-byte aligned.
+ *              The arrays are read during the call only; layers may share
+ *              matrices.
+ *   n_layers   >= 1.
+ *   hidden, ffn  multiples of 256, hidden * ffn < 2^40.
+ *   n_streams  1..4.
+ *   eps        finite, >= 0 (else PTI_ERR_VALUE).
+ *   x_in       [n_streams][hidden] fp32, 16-byte aligned; read by the first
+ *              layer only.
+ *   x_out      [n_streams][hidden] fp32 out, 4-byte aligned, overlapping no
+ *              weight matrix; may be x_in (in place).
+ *   workspace  at least pti_mlp_decode_pass_workspace_bytes(hidden, ffn,
+ *              n_streams) bytes, 256-byte aligned, overlapping no argument,
+ *              zero-filled before its first use.  The pass keeps h, each
+ *              layer's output and per-tile sums of squares there and clears
+ *              them before it ends, so every call that completes leaves the
+ *              workspace zero-filled (one workspace may serve this call and the
+ *              GEMVs above, ordered in one stream).
+ * Work: 2 n_layers + 1 kernels.  Per layer, one kernel streams W_gate and W_up
+ * together (64 gate rows and their 64 up rows per tile) and writes
+ * SiLU(g) * u; one kernel streams W_down and applies h's RMS scale to its
+ * output; each writes per-tile sums of squares of its output, from which the
+ * next kernel takes the RMS scale of its input (W (c v) = c (W v), so no
+ * separate normalisation pass over the vectors is needed).  A last kernel
+ * applies the final RMS scale.  Kernels after the first start early
+ * (programmatic dependent launch) and prefetch weights while the previous
+ * one finishes; the first waits for all earlier work in the stream.
+ * Arithmetic: GEMVs as in the conventions, SiLU with expf, RMS scales in
+ * double from fp32 per-tile sums of squares; bit-reproducible run to run.
+ */
+size_t pti_mlp_decode_pass_workspace_bytes(int64_t hidden, int64_t ffn, int n_streams);
+
+pti_status pti_mlp_decode_pass(const void *const *w_gate, const void *const *w_up, const void *const *w_down,
+                               int n_layers, int64_t hidden, int64_t ffn, int n_streams, double eps,
+                               const float *x_in, float *x_out,
+                               void *workspace, size_t workspace_bytes,
+                               pti_stream_t stream);
 
 /*
  * Reads and clears the device error word of the current device (a blocking

@@ -12,6 +12,7 @@ Functions (same names as the C ABI, without the ``pti_`` prefix):
 * ``q8_gemv_nstream(w, rows, cols, x)``      -> y [n][rows]
 * ``ssq_twin_gemv(w, rows, cols, x_a, x_b)``  -> (y_a, y_b)
 * ``verify_greedy(logits, guess)``            -> (argmax, match, accept_len)
+* ``mlp_decode_pass(w_gate, w_up, w_down, hidden, ffn, x)`` -> x after the layers
 * ``device_error()``                          -> device error word (0 = none)
 * ``lib()``                                   -> the ctypes handle of the C ABI
 """
@@ -28,6 +29,7 @@ PTI_OK = 0
 STATUS_NAMES = {
     0: "PTI_OK", 1: "PTI_ERR_NULL", 2: "PTI_ERR_SHAPE", 3: "PTI_ERR_NSTREAMS",
     4: "PTI_ERR_ALIGN", 5: "PTI_ERR_ALIAS", 6: "PTI_ERR_CUDA", 7: "PTI_ERR_WORKSPACE",
+    8: "PTI_ERR_VALUE",
 }
 
 
@@ -73,6 +75,10 @@ def lib() -> ctypes.CDLL:
             L.pti_q8_gemv_noalloc_max_scratch_bytes.argtypes = []
             L.pti_q8_gemv_nstream_noalloc.restype = I
             L.pti_q8_gemv_nstream_noalloc.argtypes = [P, I64, I64, I, P, P, P]
+            L.pti_mlp_decode_pass_workspace_bytes.restype = SZ
+            L.pti_mlp_decode_pass_workspace_bytes.argtypes = [I64, I64, I]
+            L.pti_mlp_decode_pass.restype = I
+            L.pti_mlp_decode_pass.argtypes = [P, P, P, I, I64, I64, I, ctypes.c_double, P, P, P, SZ, P]
             L.pti_device_error.restype = I
             L.pti_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             _lib = L
@@ -183,6 +189,48 @@ def q8_gemv_nstream_noalloc(w, rows: int, cols: int, x, y=None, stream=None):
     _check(lib().pti_q8_gemv_nstream_noalloc(_ptr(w), rows, cols, n, _ptr(x), _ptr(y), _stream(stream)),
            "pti_q8_gemv_nstream_noalloc")
     return y
+
+
+def mlp_decode_pass_workspace_bytes(hidden: int, ffn: int, n_streams: int) -> int:
+    return lib().pti_mlp_decode_pass_workspace_bytes(hidden, ffn, n_streams)
+
+
+def _ptr_array(tensors):
+    arr = (ctypes.c_void_p * len(tensors))(*[t.data_ptr() for t in tensors])
+    return arr
+
+
+class DecodeWeights:
+    """The host pointer arrays of a decode pass's layers (built once, reused
+    by every call; holds references to the weight tensors)."""
+
+    def __init__(self, w_gate, w_up, w_down):
+        if not (len(w_gate) == len(w_up) == len(w_down)) or len(w_gate) == 0:
+            raise ValueError("DecodeWeights: need the same number (>= 1) of gate, up and down matrices")
+        self.tensors = (list(w_gate), list(w_up), list(w_down))
+        self.gate = _ptr_array(self.tensors[0])
+        self.up = _ptr_array(self.tensors[1])
+        self.down = _ptr_array(self.tensors[2])
+        self.n_layers = len(w_gate)
+
+
+def mlp_decode_pass(weights, hidden: int, ffn: int, x, eps: float = 1e-6, x_out=None, ws=None, stream=None):
+    """Runs the gated-MLP layers of ``weights`` (a ``DecodeWeights``) over the
+    streams x [n][hidden] and returns x_out [n][hidden]."""
+    import torch
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    n = x.shape[0]
+    if x_out is None:
+        x_out = torch.empty((n, hidden), dtype=torch.float32, device=x.device)
+    need = mlp_decode_pass_workspace_bytes(hidden, ffn, n)
+    if ws is None:
+        ws = workspace(need, x.device)
+    _check(lib().pti_mlp_decode_pass(weights.gate, weights.up, weights.down, weights.n_layers, hidden, ffn, n,
+                                     float(eps), _ptr(x), _ptr(x_out), _ptr(ws),
+                                     0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+           "pti_mlp_decode_pass")
+    return x_out
 
 
 def device_error() -> int:

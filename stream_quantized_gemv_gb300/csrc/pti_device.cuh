@@ -65,7 +65,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // has not completed within kWaitTimeoutNs (or 2^30 polls), or, when
 // `abort_flag` is a shared-memory address other than 0, as soon as the 32-bit
 // word there becomes non-zero (another warp of the CTA recorded an error).
-__device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t abort_flag) {
+static __device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1; i < (1u << 30); ++i) {

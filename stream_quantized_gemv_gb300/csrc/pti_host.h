@@ -52,4 +52,8 @@ inline pti_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? PTI_OK : PTI_ERR_CUDA;
 }
 
+// Each translation unit with kernels keeps its own device error word; these
+// read and clear the decode pass's (pti_decode.cu).
+pti_status decode_take_device_error(unsigned int *code_out);
+
 }  // namespace pti

@@ -104,3 +104,50 @@ def test_verify_validation(L):
     assert _verify(L, logits=FAKE + 2) == 4 and _verify(L, am=FAKE + (2 << 34) + 1) == 4
     assert _verify(L, am=FAKE + 64) == 5                 # argmax overlaps logits
     assert _verify(L, acc=FAKE + (2 << 34) + 4) == 5     # accept overlaps argmax
+
+
+def _ptrs(*vals):
+    return (ctypes.c_void_p * len(vals))(*vals)
+
+
+GATE, UP, DOWN = FAKE + (5 << 34), FAKE + (6 << 34), FAKE + (7 << 34)
+
+
+def _decode(L, gate=None, up=None, down=None, layers=2, hidden=512, ffn=1024, n=4, eps=1e-6,
+            x_in=FAKE + (8 << 34), x_out=FAKE + (9 << 34), ws=FAKE + (10 << 34), ws_bytes=1 << 26):
+    gate = _ptrs(GATE, GATE + (1 << 30)) if gate is None else gate
+    up = _ptrs(UP, UP + (1 << 30)) if up is None else up
+    down = _ptrs(DOWN, DOWN + (1 << 30)) if down is None else down
+    return L.pti_mlp_decode_pass(gate, up, down, layers, hidden, ffn, n, eps, x_in, x_out, ws, ws_bytes, None)
+
+
+def test_decode_pass_workspace_query(L):
+    need = L.pti_mlp_decode_pass_workspace_bytes(5120, 17408, 4)
+    # stream-K partials, h, the raw layer output and the sums of squares
+    assert need >= 320 * 2 * 4 * 128 * 4 + 4 * 17408 * 4 + 4 * 5120 * 4 and need % 256 == 0
+    assert L.pti_mlp_decode_pass_workspace_bytes(5120, 17408, 1) < need
+    assert L.pti_mlp_decode_pass_workspace_bytes(5000, 17408, 4) == 0      # hidden % 256
+    assert L.pti_mlp_decode_pass_workspace_bytes(5120, 100, 4) == 0
+    assert L.pti_mlp_decode_pass_workspace_bytes(5120, 17408, 5) == 0
+
+
+def test_decode_pass_validation(L):
+    """Every call below fails validation, so nothing is launched."""
+    ok_bytes = L.pti_mlp_decode_pass_workspace_bytes(512, 1024, 4)
+    assert ok_bytes > 0
+    assert _decode(L, x_in=None) == 1 and _decode(L, x_out=None) == 1
+    assert _decode(L, gate=_ptrs(GATE, None)) == 1
+    assert L.pti_mlp_decode_pass(None, _ptrs(UP), _ptrs(DOWN), 1, 512, 1024, 4, 1e-6,
+                                 FAKE, FAKE + (1 << 30), FAKE + (2 << 30), 1 << 26, None) == 1
+    assert _decode(L, layers=0) == 2 and _decode(L, hidden=500) == 2 and _decode(L, ffn=1000) == 2
+    assert _decode(L, hidden=128) == 2
+    assert _decode(L, n=0) == 3 and _decode(L, n=5) == 3
+    assert _decode(L, eps=-1.0) == 8 and _decode(L, eps=float("nan")) == 8 and _decode(L, eps=float("inf")) == 8
+    assert _decode(L, down=_ptrs(DOWN, DOWN + 8)) == 4          # weight not 16-byte aligned
+    assert _decode(L, x_in=FAKE + (8 << 34) + 4) == 4           # x_in needs 16 bytes
+    assert _decode(L, x_out=FAKE + (9 << 34) + 2) == 4
+    assert _decode(L, ws=None) == 7 and _decode(L, ws_bytes=ok_bytes - 1) == 7
+    assert _decode(L, ws=FAKE + (10 << 34) + 16) == 4
+    assert _decode(L, x_out=GATE + (1 << 30) + 64) == 5         # x_out inside layer 1's gate matrix
+    assert _decode(L, ws=UP) == 5                                # workspace overlaps a weight matrix
+    assert _decode(L, ws=FAKE + (8 << 34) - 256) == 5           # workspace overlaps x_in
