@@ -70,7 +70,7 @@ typedef enum pti_status {
     PTI_ERR_ALIAS = 5,     /* an output overlaps an input or another output */
     PTI_ERR_CUDA = 6,      /* the CUDA runtime reported an error (no device, launch failure) */
     PTI_ERR_WORKSPACE = 7, /* workspace missing or smaller than required */
-    PTI_ERR_VALUE = 8      /* a scalar argument outside its documented range (eps) */
+    PTI_ERR_VALUE = 8      /* a scalar argument outside its documented range (eps, flags) */
 } pti_status;
 
 /* Human-readable name of a status code (static storage, never NULL). */
@@ -105,6 +105,26 @@ pti_status pti_q8_gemv_nstream(const void *w_q8, int64_t rows, int64_t cols, int
                                const float *x, float *y,
                                void *workspace, size_t workspace_bytes,
                                pti_stream_t stream);
+
+/*
+ * Launch flags of the _ex variants below (0 = the plain entry point's
+ * behaviour).
+ *   PTI_FLAG_PDL  programmatic dependent launch: the GEMV may start while the
+ *                 kernel before it in `stream` is still running.  Until that
+ *                 kernel has completed, the GEMV only reads the weight matrix
+ *                 (it fetches its first weight tiles early); it reads x and
+ *                 writes y and the workspace only afterwards.  So the caller
+ *                 promises that the preceding work in the stream does not write
+ *                 the weights.  This hides most of the launch and ramp-up time
+ *                 of a GEMV that follows another kernel (a decode step's chain
+ *                 of GEMVs).  Other flag bits return PTI_ERR_VALUE.
+ */
+#define PTI_FLAG_PDL 0x1u
+
+pti_status pti_q8_gemv_nstream_ex(const void *w_q8, int64_t rows, int64_t cols, int n_streams,
+                                  const float *x, float *y,
+                                  void *workspace, size_t workspace_bytes,
+                                  pti_stream_t stream, uint32_t flags);
 
 /*
  * Allocation-free N-stream Q8 GEMV.  The pages have no counterpart: this is a
@@ -151,6 +171,12 @@ pti_status pti_ssq_twin_gemv(const void *w_twin, int64_t rows, int64_t cols,
                              const float *x_a, const float *x_b, float *y_a, float *y_b,
                              void *workspace, size_t workspace_bytes,
                              pti_stream_t stream);
+
+/* pti_ssq_twin_gemv with launch flags (PTI_FLAG_PDL, see above). */
+pti_status pti_ssq_twin_gemv_ex(const void *w_twin, int64_t rows, int64_t cols,
+                                const float *x_a, const float *x_b, float *y_a, float *y_b,
+                                void *workspace, size_t workspace_bytes,
+                                pti_stream_t stream, uint32_t flags);
 
 /*
  * Greedy verify.

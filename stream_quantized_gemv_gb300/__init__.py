@@ -65,6 +65,10 @@ def lib() -> ctypes.CDLL:
             L.pti_q8_gemv_workspace_bytes.argtypes = [I64, I64, I]
             L.pti_q8_gemv_nstream.restype = I
             L.pti_q8_gemv_nstream.argtypes = [P, I64, I64, I, P, P, P, SZ, P]
+            L.pti_q8_gemv_nstream_ex.restype = I
+            L.pti_q8_gemv_nstream_ex.argtypes = [P, I64, I64, I, P, P, P, SZ, P, ctypes.c_uint32]
+            L.pti_ssq_twin_gemv_ex.restype = I
+            L.pti_ssq_twin_gemv_ex.argtypes = [P, I64, I64, P, P, P, P, P, SZ, P, ctypes.c_uint32]
             L.pti_ssq_twin_gemv_workspace_bytes.restype = SZ
             L.pti_ssq_twin_gemv_workspace_bytes.argtypes = [I64, I64]
             L.pti_ssq_twin_gemv.restype = I
@@ -127,8 +131,13 @@ def ssq_twin_gemv_workspace_bytes(rows: int, cols: int) -> int:
     return lib().pti_ssq_twin_gemv_workspace_bytes(rows, cols)
 
 
-def q8_gemv_nstream(w, rows: int, cols: int, x, y=None, ws=None, stream=None):
-    """y[s] = W x[s] for the n = x.shape[0] streams (1..4).  ``w``: uint8 Q8 bytes."""
+FLAG_PDL = 0x1
+
+
+def q8_gemv_nstream(w, rows: int, cols: int, x, y=None, ws=None, stream=None, flags: int = 0):
+    """y[s] = W x[s] for the n = x.shape[0] streams (1..4).  ``w``: uint8 Q8 bytes.
+    ``flags=FLAG_PDL`` lets the kernel start while the previous kernel in the
+    stream runs (that kernel must not write ``w``)."""
     import torch
     if x.dim() == 1:
         x = x.unsqueeze(0)
@@ -138,13 +147,13 @@ def q8_gemv_nstream(w, rows: int, cols: int, x, y=None, ws=None, stream=None):
     need = q8_gemv_workspace_bytes(rows, cols, n)
     if ws is None:
         ws = workspace(need, x.device)
-    _check(lib().pti_q8_gemv_nstream(_ptr(w), rows, cols, n, _ptr(x), _ptr(y), _ptr(ws),
-                                     0 if ws is None else ws.numel() * ws.element_size(),
-                                     _stream(stream)), "pti_q8_gemv_nstream")
+    _check(lib().pti_q8_gemv_nstream_ex(_ptr(w), rows, cols, n, _ptr(x), _ptr(y), _ptr(ws),
+                                        0 if ws is None else ws.numel() * ws.element_size(),
+                                        _stream(stream), flags), "pti_q8_gemv_nstream")
     return y
 
 
-def ssq_twin_gemv(w, rows: int, cols: int, x_a, x_b, y_a=None, y_b=None, ws=None, stream=None):
+def ssq_twin_gemv(w, rows: int, cols: int, x_a, x_b, y_a=None, y_b=None, ws=None, stream=None, flags: int = 0):
     """(y_A, y_B) = (W_A x_A, W_B x_B) from one packed twin matrix ``w`` (uint8)."""
     import torch
     if y_a is None:
@@ -154,9 +163,9 @@ def ssq_twin_gemv(w, rows: int, cols: int, x_a, x_b, y_a=None, y_b=None, ws=None
     need = ssq_twin_gemv_workspace_bytes(rows, cols)
     if ws is None:
         ws = workspace(need, x_a.device)
-    _check(lib().pti_ssq_twin_gemv(_ptr(w), rows, cols, _ptr(x_a), _ptr(x_b), _ptr(y_a), _ptr(y_b),
-                                   _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
-                                   _stream(stream)), "pti_ssq_twin_gemv")
+    _check(lib().pti_ssq_twin_gemv_ex(_ptr(w), rows, cols, _ptr(x_a), _ptr(x_b), _ptr(y_a), _ptr(y_b),
+                                      _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                                      _stream(stream), flags), "pti_ssq_twin_gemv")
     return y_a, y_b
 
 

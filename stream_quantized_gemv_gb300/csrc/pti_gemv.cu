@@ -130,9 +130,11 @@ extern "C" size_t pti_ssq_twin_gemv_workspace_bytes(int64_t rows, int64_t cols) 
   return fast_workspace_bytes<Fmt::Twin>(rows, 2);
 }
 
-extern "C" pti_status pti_q8_gemv_nstream(const void *w_q8, int64_t rows, int64_t cols, int n_streams,
-                                          const float *x, float *y, void *workspace, size_t workspace_bytes,
-                                          pti_stream_t stream) {
+namespace {
+pti_status q8_gemv(const void *w_q8, int64_t rows, int64_t cols, int n_streams, const float *x, float *y,
+                   void *workspace, size_t workspace_bytes, pti_stream_t stream, uint32_t flags) {
+  if ((flags & ~PTI_FLAG_PDL) != 0u) return PTI_ERR_VALUE;
+  const bool pdl = (flags & PTI_FLAG_PDL) != 0u;
   if (w_q8 == nullptr || x == nullptr || y == nullptr) return PTI_ERR_NULL;
   if (const pti_status s = check_gemv_shape(rows, cols); s != PTI_OK) return s;
   if (n_streams < 1 || n_streams > 4) return PTI_ERR_NSTREAMS;
@@ -152,10 +154,10 @@ extern "C" pti_status pti_q8_gemv_nstream(const void *w_q8, int64_t rows, int64_
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (need > 0 && aligned(x, 16)) {
     switch (n_streams) {
-      case 1: return launch_fast<Fmt::Q8, 1>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st);
-      case 2: return launch_fast<Fmt::Q8, 2>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st);
-      case 3: return launch_fast<Fmt::Q8, 3>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st);
-      default: return launch_fast<Fmt::Q8, 4>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st);
+      case 1: return launch_fast<Fmt::Q8, 1>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st, pdl);
+      case 2: return launch_fast<Fmt::Q8, 2>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st, pdl);
+      case 3: return launch_fast<Fmt::Q8, 3>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st, pdl);
+      default: return launch_fast<Fmt::Q8, 4>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st, pdl);
     }
   }
   switch (n_streams) {
@@ -166,9 +168,10 @@ extern "C" pti_status pti_q8_gemv_nstream(const void *w_q8, int64_t rows, int64_
   }
 }
 
-extern "C" pti_status pti_ssq_twin_gemv(const void *w_twin, int64_t rows, int64_t cols, const float *x_a,
-                                        const float *x_b, float *y_a, float *y_b, void *workspace,
-                                        size_t workspace_bytes, pti_stream_t stream) {
+pti_status twin_gemv(const void *w_twin, int64_t rows, int64_t cols, const float *x_a, const float *x_b, float *y_a,
+                     float *y_b, void *workspace, size_t workspace_bytes, pti_stream_t stream, uint32_t flags) {
+  if ((flags & ~PTI_FLAG_PDL) != 0u) return PTI_ERR_VALUE;
+  const bool pdl = (flags & PTI_FLAG_PDL) != 0u;
   if (w_twin == nullptr || x_a == nullptr || x_b == nullptr || y_a == nullptr || y_b == nullptr)
     return PTI_ERR_NULL;
   if (const pti_status s = check_gemv_shape(rows, cols); s != PTI_OK) return s;
@@ -192,7 +195,7 @@ extern "C" pti_status pti_ssq_twin_gemv(const void *w_twin, int64_t rows, int64_
         overlaps(workspace, need, y_b, y_bytes))
       return PTI_ERR_ALIAS;
     if (aligned(x_a, 16) && aligned(x_b, 16))
-      return launch_fast<Fmt::Twin, 2>(w_twin, rows, cols, x_a, x_b, y_a, y_b, workspace, st);
+      return launch_fast<Fmt::Twin, 2>(w_twin, rows, cols, x_a, x_b, y_a, y_b, workspace, st, pdl);
   }
   const int sms = current_device_sms();
   if (sms <= 0) return PTI_ERR_CUDA;
@@ -200,6 +203,32 @@ extern "C" pti_status pti_ssq_twin_gemv(const void *w_twin, int64_t rows, int64_
   twin_rowwise_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<const uint8_t *>(w_twin), rows, cols,
                                                                      x_a, x_b, y_a, y_b);
   return launch_status();
+}
+
+}  // namespace
+
+extern "C" pti_status pti_q8_gemv_nstream(const void *w_q8, int64_t rows, int64_t cols, int n_streams,
+                                          const float *x, float *y, void *workspace, size_t workspace_bytes,
+                                          pti_stream_t stream) {
+  return q8_gemv(w_q8, rows, cols, n_streams, x, y, workspace, workspace_bytes, stream, 0u);
+}
+
+extern "C" pti_status pti_q8_gemv_nstream_ex(const void *w_q8, int64_t rows, int64_t cols, int n_streams,
+                                             const float *x, float *y, void *workspace, size_t workspace_bytes,
+                                             pti_stream_t stream, uint32_t flags) {
+  return q8_gemv(w_q8, rows, cols, n_streams, x, y, workspace, workspace_bytes, stream, flags);
+}
+
+extern "C" pti_status pti_ssq_twin_gemv(const void *w_twin, int64_t rows, int64_t cols, const float *x_a,
+                                        const float *x_b, float *y_a, float *y_b, void *workspace,
+                                        size_t workspace_bytes, pti_stream_t stream) {
+  return twin_gemv(w_twin, rows, cols, x_a, x_b, y_a, y_b, workspace, workspace_bytes, stream, 0u);
+}
+
+extern "C" pti_status pti_ssq_twin_gemv_ex(const void *w_twin, int64_t rows, int64_t cols, const float *x_a,
+                                           const float *x_b, float *y_a, float *y_b, void *workspace,
+                                           size_t workspace_bytes, pti_stream_t stream, uint32_t flags) {
+  return twin_gemv(w_twin, rows, cols, x_a, x_b, y_a, y_b, workspace, workspace_bytes, stream, flags);
 }
 
 // ---------------------------------------------------------------------------

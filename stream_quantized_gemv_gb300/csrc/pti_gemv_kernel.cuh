@@ -20,14 +20,16 @@
 //    number of bytes.  Row tiles shared by several CTAs are combined by the
 //    last CTA to finish them (an atomic ticket per tile, partials in a
 //    caller-supplied workspace, summed in a fixed CTA order).
-//  * One producer warp issues the copies into a ring of up to 6 stages guarded
-//    by mbarriers; 16 consumer warps compute.  Lane l of a consumer task owns
-//    two rows of the tile and reads its 16-byte chunk of each with one aligned,
-//    bank-conflict-free shared load.  The 17 chunk positions fall into a few
-//    structural classes (where the block scale sits in the chunk), one code
-//    body per class; scheduler k owns chunks k, k+4, k+8, k+12 (chunk 16
-//    rotates over the schedulers from unit to unit) and its four warps split
-//    each owned chunk into two 64-row halves.
+//  * Lane 0 of consumer warp 0 issues the copies into a ring of up to 6 stages
+//    guarded by mbarriers (it refills a slot once every warp has released
+//    it); 16 warps compute.  Q8: warp w always computes block w % 8 of each
+//    unit for 64 rows (two per lane), reading each row's 48-byte window around
+//    the block with three aligned, conflict-free 16-byte loads; the four warps
+//    of a scheduler share one code body.  Twin: lane l of a task owns two rows
+//    and reads its 16-byte chunk of each; the 17 chunk positions fall into a
+//    few structural classes (where the block scale sits in the chunk), one
+//    code body per class; scheduler k owns chunks k, k+4, k+8, k+12 (chunk 16
+//    rotates over the schedulers from unit to unit).
 //  * Each stage also holds the unit's slice of the activations (N x 1 KB,
 //    stream-major), fetched by one bulk copy per stream next to the weight
 //    tile.  Every warp reads them with broadcast loads and reuses them for its
@@ -300,6 +302,67 @@ __device__ __forceinline__ void twin_body(const uint8_t *tile, const ChunkParams
   }
 }
 
+// One Q8 block b of the super-block (columns 32b .. 32b+31) for the lane's
+// two rows of half h.  The block's 34 bytes lie in the 48-byte window that
+// starts at byte 32b of the row (three aligned 16-byte loads, conflict-free
+// since rows are 272 bytes apart), from window byte 2b on.  With b = 2c + e,
+// the block starts in window word c at half-word e: the words c .. c+8 are
+// moved to the front by two selects on c (b is fixed per warp, so the
+// predicates are loop-invariant), after which only the parity e decides where
+// each byte sits: the scale is half-word e of word 0, weight pair j (columns
+// 32b+2j, 32b+2j+1) is at byte 2e+2+2j.  One code body per parity keeps the
+// instruction footprint of all warps small.
+template <int N, int E, int CLO>
+__device__ __forceinline__ void q8_block_body(const uint8_t *tile, const uint8_t *xblk, uint32_t lane, uint32_t half,
+                                              uint32_t win_off, bool c_hi, uint64_t (&acc)[kTaskSlots][N]) {
+  uint32_t w[kTaskSlots][9];
+  ScalePair sc[kTaskSlots];
+#pragma unroll
+  for (int r = 0; r < kTaskSlots; ++r) {
+    const uint8_t *win = tile + (half * 64 + r * 32 + lane) * kSBBytes + win_off;
+    const uint4 v0 = *reinterpret_cast<const uint4 *>(win);
+    const uint4 v1 = *reinterpret_cast<const uint4 *>(win + 16);
+    const uint4 v2 = *reinterpret_cast<const uint4 *>(win + 32);
+    const uint32_t words[12] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w, v2.x, v2.y, v2.z, v2.w};
+    uint32_t t1[10];
+#pragma unroll
+    for (int k = 0; k < 10; ++k) t1[k] = c_hi ? words[k + 2] : words[k];
+#pragma unroll
+    for (int k = 0; k < 9; ++k) w[r][k] = t1[k + CLO];
+    sc[r] = make_scale(E ? (w[r][0] >> 16) : (w[r][0] & 0xFFFFu));
+#pragma unroll
+    for (int k = 0; k < 9; ++k) w[r][k] ^= 0x80808080u;
+  }
+  uint64_t p[kTaskSlots][N];
+  static_for<0, 8>([&](auto jc) {  // two weight pairs per step: one 16-byte x load per stream
+    constexpr int j0 = 2 * decltype(jc)::value;
+    ulonglong2 xv[N];
+#pragma unroll
+    for (int st = 0; st < N; ++st)
+      xv[st] = *reinterpret_cast<const ulonglong2 *>(xblk + st * Stage<Fmt::Q8, N>::kXStreamBytes + j0 * 8);
+    static_for<0, 2>([&](auto jj_) {
+      constexpr int j = j0 + decltype(jj_)::value;
+      constexpr int t = 2 * E + 2 + 2 * j;  // byte of the pair's first weight in the aligned words
+#pragma unroll
+      for (int r = 0; r < kTaskSlots; ++r) {
+        const uint64_t wq = dequant2(w[r][t / 4], t % 4, w[r][t / 4], t % 4 + 1, sc[r]);
+        static_for<0, N>([&](auto sc_) {
+          constexpr int st = decltype(sc_)::value;
+          const uint64_t xs = (j & 1) ? xv[st].y : xv[st].x;
+          if constexpr (j == 0) p[r][st] = fmul2(wq, xs);
+          else p[r][st] = ffma2(wq, xs, p[r][st]);
+        });
+      }
+    });
+  });
+#pragma unroll
+  for (int r = 0; r < kTaskSlots; ++r)
+    static_for<0, N>([&](auto sc_) {
+      constexpr int st = decltype(sc_)::value;
+      acc[r][st] = fadd2(acc[r][st], p[r][st]);
+    });
+}
+
 template <Fmt F, int N>
 __device__ __forceinline__ ChunkParams chunk_params(int c) {
   if constexpr (F == Fmt::Q8) return q8_chunk_params(c);
@@ -367,7 +430,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // Warp s < kOut handles vector s; must run after the wait on the previous
 // kernel.  A consumer barrier must separate it from the first reader.
 template <int kOut>
-__device__ __forceinline__ void input_scales(const GemvArgs &a, uint32_t warp, uint32_t lane, float *scale) {
+__device__ __noinline__ void input_scales(const GemvArgs &a, uint32_t warp, uint32_t lane, float *scale) {
   if (warp >= static_cast<uint32_t>(kOut)) return;
   double s2 = 0.0;
   if (a.sq_in != nullptr)
@@ -430,91 +493,301 @@ __device__ __forceinline__ void down_epilogue(const GemvArgs &a, const float *ti
         (wsum[4 * tid] + wsum[4 * tid + 1]) + (wsum[4 * tid + 2] + wsum[4 * tid + 3]);
 }
 
-// Sums the 16 warps' partials of one deferred row-tile segment (red slot `sl`)
-// into the tile's totals: straight to the output (Plain) or the epilogue's
-// tile buffer when no other CTA shares the tile, else as this CTA's partial,
-// the last CTA to finish the tile adding all partials in CTA order.  The
-// fused epilogues then run on the complete tile.
+// Consumer warp q (0..7) of the warps that computed half h of a tile.  Q8:
+// warp w covers block w % 8 of half w / 8; twin: warp w covers half (w / 4) % 2.
+template <Fmt F>
+__device__ __forceinline__ int red_warp(int q, int h) {
+  if constexpr (F == Fmt::Q8) return 8 * h + q;
+  else return (q >> 2) * 8 + h * 4 + (q & 3);
+}
+
+// Finishes one or two row tiles of the CTA: tile k (row tile rb[k], deferred
+// warp sums in red slot sl[k]).  Each element's total is the tree sum of the 8
+// warps that computed it.  A tile no other CTA shares is written out directly
+// (Plain) or through the fused epilogue.  A shared tile's totals go to this
+// CTA's partial slot in the workspace; after one fence and one ticket per
+// tile (both tiles in the same round, so the round trips to L2 overlap), the
+// last CTA to arrive at a tile adds the partials of all its CTAs in CTA order
+// and writes the result; the others are done with it.
+// Not inlined: it runs a few times per CTA, and one shared copy keeps the
+// consumer loops' instruction footprint small.
 template <Fmt F, int N, Epi E>
-__device__ __forceinline__ void finish_tile(const GemvArgs &a, const float *red, int sl, int32_t rb, uint32_t tid,
-                                            volatile uint32_t *flag, float *epi) {
+__device__ __noinline__ void finish_tiles(const GemvArgs &a, const float *red, int count, int32_t rb0, int sl0,
+                                          int32_t rb1, int sl1, uint32_t tid, volatile uint32_t *flag, float *epi) {
   using T = Traits<F, N>;
   constexpr int kOut = T::kOut;
   constexpr int kConsumerThreads = T::kWarps * 32;
-  float *const tile_out = epi;                                // [kOut][128]
-  float *const scale = epi + 4 * kRowsPerTile;                // [kOut]
-  float *const wsum = scale + 4;                              // [16]
-  const int32_t c_lo = cta_of_unit(static_cast<int64_t>(rb) * a.n_sb, a.units, a.grid);
-  const int32_t c_hi = cta_of_unit(static_cast<int64_t>(rb + 1) * a.n_sb - 1, a.units, a.grid);
-  const bool shared_tile = c_hi > c_lo;
-  auto deliver = [&](int s, int row, float total) {
-    if constexpr (E == Epi::Plain) {
-      const int64_t row_g = static_cast<int64_t>(rb) * kRowsPerTile + row;
-      if (row_g < a.rows) {
-        if constexpr (F == Fmt::Q8) a.y0[s * a.rows + row_g] = total;
-        else (s == 0 ? a.y0 : a.y1)[row_g] = total;
-      }
-    } else {
-      tile_out[s * kRowsPerTile + row] = total;
-    }
-  };
-  for (int t = tid; t < kOut * kRowsPerTile; t += kConsumerThreads) {
-    const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
+  float *const tile_out = epi;                  // [kOut][128]
+  float *const scale = epi + 4 * kRowsPerTile;  // [kOut]
+  float *const wsum = scale + 4;                // [16]
+  const int32_t rbs[2] = {rb0, rb1};
+  const int sls[2] = {sl0, sl1};
+  int32_t clo[2] = {0, 0}, chi[2] = {0, 0};
+  bool any_shared = false;
+  for (int k = 0; k < count; ++k) {
+    clo[k] = cta_of_unit(static_cast<int64_t>(rbs[k]) * a.n_sb, a.units, a.grid);
+    chi[k] = cta_of_unit(static_cast<int64_t>(rbs[k] + 1) * a.n_sb - 1, a.units, a.grid);
+    any_shared = any_shared || chi[k] > clo[k];
+  }
+  auto warp_total = [&](int k, int s, int row) {
     float v[T::kWarps / 2];
 #pragma unroll
-    for (int q = 0; q < T::kWarps / 2; ++q) {
-      const int w = (q >> 2) * 8 + (row >> 6) * 4 + (q & 3);  // the warps whose half is row / 64
-      v[q] = red[((sl * T::kWarps + w) * kOut + s) * 64 + (row & 63)];
+    for (int q = 0; q < T::kWarps / 2; ++q)
+      v[q] = red[((sls[k] * T::kWarps + red_warp<F>(q, row >> 6)) * kOut + s) * 64 + (row & 63)];
+    return tree_sum(v);
+  };
+  auto part_slot = [&](int32_t cta, int slot, int s, int row) {
+    return &a.part[((static_cast<int64_t>(cta) * 2 + slot) * kOut + s) * kRowsPerTile + row];
+  };
+  // ---- shared tiles: publish this CTA's partials, one ticket round for all
+  uint32_t last_bits = 0;
+  if (any_shared) {
+    for (int k = 0; k < count; ++k) {
+      if (chi[k] == clo[k]) continue;
+      for (int t = tid; t < kOut * kRowsPerTile; t += kConsumerThreads) {
+        const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
+        *part_slot(static_cast<int32_t>(blockIdx.x), sls[k], s, row) = warp_total(k, s, row);
+      }
     }
-    const float total = tree_sum(v);
-    if (!shared_tile) deliver(s, row, total);
-    else a.part[((static_cast<int64_t>(blockIdx.x) * 2 + sl) * kOut + s) * kRowsPerTile + row] = total;
-  }
-  if (shared_tile) {
     __threadfence();
     named_barrier(kBarConsumers, kConsumerThreads);
     if (tid == 0) {
-      const unsigned int prev = atomicAdd(&a.tickets[rb], 1u);
-      const bool last = prev == static_cast<unsigned int>(c_hi - c_lo);
-      if (last) {
-        a.tickets[rb] = 0u;  // leave the workspace zeroed for the next call
-        __threadfence();
+      uint32_t bits = 0;
+      for (int k = 0; k < count; ++k) {
+        if (chi[k] == clo[k]) continue;
+        const unsigned int prev = atomicAdd(&a.tickets[rbs[k]], 1u);
+        if (prev == static_cast<unsigned int>(chi[k] - clo[k])) {
+          a.tickets[rbs[k]] = 0u;  // leave the workspace zeroed for the next call
+          bits |= 1u << k;
+        }
       }
-      flag[1] = last ? 1u : 0u;
+      if (bits != 0u) __threadfence();
+      flag[1] = bits;
     }
     named_barrier(kBarConsumers, kConsumerThreads);
-    if (flag[1] == 0) return;
+    last_bits = flag[1];
+  }
+  // ---- write out the tiles this CTA completes
+  bool epilogue_ran = false;
+  for (int k = 0; k < count; ++k) {
+    const bool shared_tile = chi[k] > clo[k];
+    if (shared_tile && ((last_bits >> k) & 1u) == 0u) continue;
+    if constexpr (E != Epi::Plain)
+      if (epilogue_ran) named_barrier(kBarConsumers, kConsumerThreads);  // tile_out and wsum are reused
     for (int t = tid; t < kOut * kRowsPerTile; t += kConsumerThreads) {
       const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
-      float total = 0.0f;
-      for (int32_t c = c_lo; c <= c_hi; ++c) {
-        const int cs = (rb == first_tile_of_cta(c, a.units, a.grid, a.n_sb)) ? 0 : 1;
-        float *const slot_ptr = &a.part[((static_cast<int64_t>(c) * 2 + cs) * kOut + s) * kRowsPerTile + row];
-        const float v = __ldcg(slot_ptr);
-        *slot_ptr = 0.0f;  // the whole workspace is zero again when the call completes
-        total = (c == c_lo) ? v : total + v;
+      float total;
+      if (!shared_tile) {
+        total = warp_total(k, s, row);
+      } else {
+        total = 0.0f;
+        for (int32_t c = clo[k]; c <= chi[k]; ++c) {
+          const int cs = (rbs[k] == first_tile_of_cta(c, a.units, a.grid, a.n_sb)) ? 0 : 1;
+          float *const slot_ptr = part_slot(c, cs, s, row);
+          const float v = __ldcg(slot_ptr);
+          *slot_ptr = 0.0f;  // the whole workspace is zero again when the call completes
+          total = (c == clo[k]) ? v : total + v;
+        }
       }
-      deliver(s, row, total);
+      if constexpr (E == Epi::Plain) {
+        const int64_t row_g = static_cast<int64_t>(rbs[k]) * kRowsPerTile + row;
+        if (row_g < a.rows) {
+          if constexpr (F == Fmt::Q8) a.y0[s * a.rows + row_g] = total;
+          else (s == 0 ? a.y0 : a.y1)[row_g] = total;
+        }
+      } else {
+        tile_out[s * kRowsPerTile + row] = total;
+      }
+    }
+    if constexpr (E != Epi::Plain) {
+      named_barrier(kBarConsumers, kConsumerThreads);
+      if constexpr (E == Epi::GateUp) gateup_epilogue<kOut>(a, tile_out, scale, wsum, rbs[k], tid, kConsumerThreads);
+      else down_epilogue<kOut>(a, tile_out, scale, wsum, rbs[k], tid, kConsumerThreads);
+      epilogue_ran = true;
     }
   }
-  if constexpr (E != Epi::Plain) {
-    named_barrier(kBarConsumers, kConsumerThreads);
-    if constexpr (E == Epi::GateUp) gateup_epilogue<kOut>(a, tile_out, scale, wsum, rb, tid, kConsumerThreads);
-    else down_epilogue<kOut>(a, tile_out, scale, wsum, rb, tid, kConsumerThreads);
-  }
 }
+
+// Shared-memory layout and identity of a consumer thread.
+struct ConsumerCtx {
+  uint8_t *base_ptr;        // ring of stages
+  float *red;               // [2 slots][warps][kOut][64] deferred warp sums
+  float *epi;               // fused-epilogue scratch
+  volatile uint32_t *flag;  // [0] abort, [1] last-arriver flag
+  uint32_t bars, flags;     // shared addresses of the barriers and flags
+  int stages;
+  uint32_t tid, warp, lane;
+  int64_t u0, u1;           // this CTA's unit range
+};
+
+// The consumer warps' walk over the CTA's units: wait for each stage, run
+// `body` on it (the warp's share of the unit), release the stage; at the end
+// of each row tile park the warp's sums, and finish the tiles.
+template <Fmt F, int N, Epi E, class Body, class Release>
+__device__ __forceinline__ void consumer_loop(const GemvArgs &a, const ConsumerCtx &c, Body &&body, Release &&release) {
+  using T = Traits<F, N>;
+  using S = Stage<F, N>;
+  constexpr int kOut = T::kOut;
+  constexpr int kConsumerThreads = T::kWarps * 32;
+  uint64_t acc[kTaskSlots][kOut];
+  uint32_t st = 0, ph = 0;  // ring slot and phase parity of unit i
+  int64_t i = 0;
+  const int32_t rb_first = static_cast<int32_t>(c.u0 / a.n_sb);
+  const int32_t rb_last = static_cast<int32_t>((c.u1 - 1) / a.n_sb);
+  for (int32_t rb = rb_first; rb <= rb_last; ++rb) {
+    const int32_t sb_begin = (rb == rb_first) ? static_cast<int32_t>(c.u0 - static_cast<int64_t>(rb) * a.n_sb) : 0;
+    const int32_t sb_end = (rb == rb_last) ? static_cast<int32_t>(c.u1 - static_cast<int64_t>(rb) * a.n_sb) : a.n_sb;
+#pragma unroll
+    for (int r = 0; r < kTaskSlots; ++r)
+#pragma unroll
+      for (int s = 0; s < kOut; ++s) acc[r][s] = 0ull;
+
+    for (int32_t sb = sb_begin; sb < sb_end; ++sb, ++i) {
+      const uint32_t full = c.bars + 8 * st;
+      bool ok = mbar_try_wait(full, ph);
+      if (!ok) {
+        ok = c.flag[0] == 0 && mbar_wait_bounded(full, ph, c.flags);
+        if (!ok && c.flag[0] == 0) {
+          atomicOr(&g_device_error, PTI_DEVERR_FULL_TIMEOUT);
+          c.flag[0] = 1;
+        }
+      }
+      if (ok) {
+        const uint8_t *tile = c.base_ptr + st * S::kBytes;
+        body(tile, tile + kStageBytes, i, acc);
+      }
+      __syncwarp();
+      if (c.lane == 0) mbar_arrive(c.bars + 8 * (c.stages + st));
+      release(i, st, ph);
+      if (++st == static_cast<uint32_t>(c.stages)) {
+        st = 0;
+        ph ^= 1u;
+      }
+    }
+
+    // ---- park this warp's sums for the tile: slot 0 = first tile of the CTA,
+    //      slot 1 = any later one (only the last can be shared with another CTA)
+    const int sl = (rb == rb_first) ? 0 : 1;
+    const bool middle = rb != rb_first && rb != rb_last;
+#pragma unroll
+    for (int r = 0; r < kTaskSlots; ++r)
+#pragma unroll
+      for (int s = 0; s < kOut; ++s) {
+        const float2 v = unpack2(acc[r][s]);
+        c.red[((sl * T::kWarps + c.warp) * kOut + s) * 64 + r * 32 + c.lane] = v.x + v.y;
+      }
+    if (middle) {
+      // a tile wholly inside this CTA's range: finish it now (rare: only when
+      // a CTA spans more than two row tiles)
+      named_barrier(kBarConsumers, kConsumerThreads);
+      finish_tiles<F, N, E>(a, c.red, 1, rb, 1, 0, 0, c.tid, c.flag, c.epi);
+      named_barrier(kBarConsumers, kConsumerThreads);
+    }
+  }
+  named_barrier(kBarConsumers, kConsumerThreads);
+  finish_tiles<F, N, E>(a, c.red, rb_last != rb_first ? 2 : 1, rb_first, 0, rb_last, 1, c.tid, c.flag, c.epi);
+}
+
+// The copy side of the ring, run by lane 0 of the producer warp: it fills the
+// first stages at start and refills each slot as soon as every consumer warp
+// has released it.  (Folding this into a consumer warp frees a warp and
+// raises the register budget from 96 to 128 per thread, but the consumer that
+// refills then waits for the slowest warp on every unit; measured slower.)
+template <Fmt F, int N, Epi E>
+struct Producer {
+  using T = Traits<F, N>;
+  using S = Stage<F, N>;
+  const CUtensorMap *tmap, *tmap2;
+  const GemvArgs *a;
+  uint32_t base, bars, flags;
+  volatile uint32_t *flag;
+  int stages;
+  int64_t u0, nu, issued;
+  uint64_t pol;
+
+  __device__ __forceinline__ void coords(int64_t i, int32_t &rb, int32_t &sb) const {
+    const int64_t u = u0 + i;
+    rb = static_cast<int32_t>(u / a->n_sb);
+    sb = static_cast<int32_t>(u - static_cast<int64_t>(rb) * a->n_sb);
+  }
+  __device__ __forceinline__ void load_w(int64_t i, uint32_t slot) const {
+    int32_t rb, sb;
+    coords(i, rb, sb);
+    const uint32_t dst = base + slot * S::kBytes, bar = bars + 8 * slot;
+    if constexpr (E == Epi::GateUp) {
+      tma_load_2d(dst, tmap, 34 * sb, rb * 64, bar, pol);
+      tma_load_2d(dst + 64 * kSBBytes, tmap2, 34 * sb, rb * 64, bar, pol);
+    } else {
+      tma_load_2d(dst, tmap, 34 * sb, rb * kRowsPerTile, bar, pol);
+    }
+  }
+  __device__ __forceinline__ void load_x(int64_t i, uint32_t slot) const {
+    int32_t rb, sb;
+    coords(i, rb, sb);
+    const uint32_t xdst = base + slot * S::kBytes + kStageBytes, bar = bars + 8 * slot;
+    if constexpr (F == Fmt::Q8) {
+#pragma unroll
+      for (int st = 0; st < N; ++st)
+        bulk_load(xdst + st * S::kXStreamBytes,
+                  a->x0 + static_cast<int64_t>(st) * a->cols + static_cast<int64_t>(sb) * T::kColsPerSB,
+                  S::kXStreamBytes, bar);
+    } else {
+      bulk_load(xdst, a->x0 + static_cast<int64_t>(sb) * T::kColsPerSB, S::kXStreamBytes, bar);
+      bulk_load(xdst + S::kXStreamBytes, a->x1 + static_cast<int64_t>(sb) * T::kColsPerSB, S::kXStreamBytes, bar);
+    }
+  }
+  // Weights do not depend on the previous kernel in the stream: fetch the
+  // first tiles before waiting for it, then their activations.
+  __device__ __forceinline__ void start() {
+    prefetch_tmap(tmap);
+    if constexpr (E == Epi::GateUp) prefetch_tmap(tmap2);
+    const int64_t pre = nu < stages ? nu : stages;
+    for (int64_t i = 0; i < pre; ++i) {
+      mbar_expect_tx(bars + 8 * i, kStageBytes);
+      load_w(i, static_cast<uint32_t>(i));
+    }
+    pdl_wait_primary();
+    for (int64_t i = 0; i < pre; ++i) {
+      mbar_arrive_expect_tx(bars + 8 * i, S::kXBytes);
+      load_x(i, static_cast<uint32_t>(i));
+    }
+    issued = pre;
+  }
+  // Once every consumer warp has released unit i (ring slot st, phase parity
+  // ph), fetch unit i + stages into the slot.
+  __device__ __forceinline__ void refill(int64_t i, uint32_t st, uint32_t ph) {
+    const int64_t j = i + stages;
+    if (j >= nu || flag[0] != 0) return;
+    const uint32_t empty = bars + 8 * (stages + st);
+    if (!mbar_try_wait(empty, ph) && !mbar_wait_bounded(empty, ph, flags)) {
+      if (flag[0] == 0) atomicOr(&g_device_error, PTI_DEVERR_EMPTY_TIMEOUT);
+      flag[0] = 1;
+      return;
+    }
+    mbar_arrive_expect_tx(bars + 8 * st, kStageBytes + S::kXBytes);
+    load_w(j, st);
+    load_x(j, st);
+    issued = j + 1;
+  }
+  // Stay until every copy issued into this CTA's shared memory has landed
+  // (they all have unless a wait gave up).
+  __device__ __forceinline__ void drain() const {
+    for (int64_t i = (issued > stages ? issued - stages : 0); i < issued; ++i)
+      if (!mbar_wait_bounded(bars + 8 * (i % stages), static_cast<uint32_t>((i / stages) & 1), 0))
+        atomicOr(&g_device_error, PTI_DEVERR_DRAIN_TIMEOUT);
+  }
+};
 
 // tmap: the weight matrix (box 34 x 8 bytes by 128 rows); GateUp: the gate
 // matrix and tmap2 the up matrix (boxes of 64 rows each).
 template <Fmt F, int N, Epi E>
 __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
     gemv_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap2,
-                    const GemvArgs a) {
+                    const __grid_constant__ GemvArgs a) {
   using T = Traits<F, N>;
   using S = Stage<F, N>;
   constexpr int kOut = T::kOut;
   constexpr int kConsumerWarps = T::kWarps;
-  constexpr int kConsumerThreads = kConsumerWarps * 32;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -545,161 +818,66 @@ __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
   if (warp == kConsumerWarps) {
     // ---------------- producer: one lane issues every copy --------------------
     if (lane == 0) {
-      prefetch_tmap(&tmap);
-      if constexpr (E == Epi::GateUp) prefetch_tmap(&tmap2);
-      const uint64_t pol = l2_policy_evict_first();
-      auto load_w = [&](uint32_t slot, int32_t rb, int32_t sb) {
-        const uint32_t dst = base + slot * S::kBytes, bar = bars + 8 * slot;
-        if constexpr (E == Epi::GateUp) {
-          tma_load_2d(dst, &tmap, 34 * sb, rb * 64, bar, pol);
-          tma_load_2d(dst + 64 * kSBBytes, &tmap2, 34 * sb, rb * 64, bar, pol);
-        } else {
-          tma_load_2d(dst, &tmap, 34 * sb, rb * kRowsPerTile, bar, pol);
-        }
-      };
-      const int64_t nu = u1 - u0;
-      const int64_t pre = nu < stages ? nu : stages;
-      auto unit_coords = [&](int64_t i, int32_t &rb, int32_t &sb) {
-        const int64_t u = u0 + i;
-        rb = static_cast<int32_t>(u / a.n_sb);
-        sb = static_cast<int32_t>(u - static_cast<int64_t>(rb) * a.n_sb);
-      };
-      auto load_x = [&](int64_t i, uint32_t slot) {
-        int32_t rb, sb;
-        unit_coords(i, rb, sb);
-        const uint32_t xdst = base + slot * S::kBytes + kStageBytes;
-        const uint32_t bar = bars + 8 * slot;
-        if constexpr (F == Fmt::Q8) {
-#pragma unroll
-          for (int st = 0; st < N; ++st)
-            bulk_load(xdst + st * S::kXStreamBytes, a.x0 + static_cast<int64_t>(st) * a.cols + static_cast<int64_t>(sb) * T::kColsPerSB,
-                      S::kXStreamBytes, bar);
-        } else {
-          bulk_load(xdst, a.x0 + static_cast<int64_t>(sb) * T::kColsPerSB, S::kXStreamBytes, bar);
-          bulk_load(xdst + S::kXStreamBytes, a.x1 + static_cast<int64_t>(sb) * T::kColsPerSB, S::kXStreamBytes, bar);
-        }
-      };
-      // Weights do not depend on the previous kernel in the stream: prefetch
-      // the first tiles before waiting for it, then fetch their activations.
-      for (int64_t i = 0; i < pre; ++i) {
-        int32_t rb, sb;
-        unit_coords(i, rb, sb);
-        mbar_expect_tx(bars + 8 * i, kStageBytes);
-        load_w(static_cast<uint32_t>(i), rb, sb);
-      }
-      pdl_wait_primary();
-      for (int64_t i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(bars + 8 * i, S::kXBytes);
-        load_x(i, static_cast<uint32_t>(i));
-      }
-      int64_t issued = pre;
-      uint32_t st = static_cast<uint32_t>(pre % stages), eph = 0;  // slot and empty-phase parity
-      for (int64_t i = pre; i < nu; ++i) {
-        const uint32_t empty = bars + 8 * (stages + st);
-        if (!mbar_try_wait(empty, eph) && !mbar_wait_bounded(empty, eph, flags)) {
-          if (flag[0] == 0) atomicOr(&g_device_error, PTI_DEVERR_EMPTY_TIMEOUT);
-          flag[0] = 1;
-          break;
-        }
-        if (flag[0] != 0) break;
-        int32_t rb, sb;
-        unit_coords(i, rb, sb);
-        mbar_arrive_expect_tx(bars + 8 * st, kStageBytes + S::kXBytes);
-        load_w(st, rb, sb);
-        load_x(i, st);
-        issued = i + 1;
+      Producer<F, N, E> prod{&tmap, &tmap2, &a, base, bars, flags, flag, stages, u0, u1 - u0, 0,
+                             l2_policy_evict_first()};
+      prod.start();
+      uint32_t st = 0, ph = 0;
+      for (int64_t i = 0; i + stages < prod.nu && flag[0] == 0; ++i) {
+        prod.refill(i, st, ph);
         if (++st == static_cast<uint32_t>(stages)) {
           st = 0;
-          eph ^= 1u;
+          ph ^= 1u;
         }
       }
-      // Stay until every copy issued into this CTA's shared memory has landed.
-      for (int64_t i = (issued > stages ? issued - stages : 0); i < issued; ++i) {
-        if (!mbar_wait_bounded(bars + 8 * (i % stages), static_cast<uint32_t>((i / stages) & 1), 0))
-          atomicOr(&g_device_error, PTI_DEVERR_DRAIN_TIMEOUT);
-      }
+      prod.drain();
     }
     return;
   }
 
   // ---------------- consumers ----------------------------------------------
-  uint64_t acc[kTaskSlots][kOut];
-  // Warp w runs on scheduler k = w % 4 (warps are dealt to the four schedulers
-  // round-robin) and always works on the same two chunks of every unit, rows
-  // of half j % 2 (j = w / 4): chunks k + 4(j/2) and k + 4(j/2) + 8, so each
-  // scheduler owns chunks k, k+4, k+8, k+12.  Chunk 16 of unit i goes to the
-  // warps j = 0, 1 of scheduler i % 4.
-  const uint32_t sched = warp & 3u, wj = warp >> 2;
-  const uint32_t half = wj & 1u;
-  const int ca = static_cast<int>(sched + 4u * (wj >> 1));
-  const ChunkParams pa = chunk_params<F, N>(ca), pb = chunk_params<F, N>(ca + 8),
-                    p16 = chunk_params<F, N>(16);
-  const bool takes16 = (wj >> 1) == 0u;
   if constexpr (E != Epi::Plain) {
     pdl_wait_primary();  // the input's sums of squares come from the previous kernel
     input_scales<kOut>(a, warp, lane, epi + 4 * kRowsPerTile);
   }
-  uint32_t st = 0, ph = 0;  // ring slot and phase parity of unit i
-  int64_t i = 0;
-  const int32_t rb_first = static_cast<int32_t>(u0 / a.n_sb);
-  const int32_t rb_last = static_cast<int32_t>((u1 - 1) / a.n_sb);
-  for (int32_t rb = rb_first; rb <= rb_last; ++rb) {
-    const int32_t sb_begin = (rb == rb_first) ? static_cast<int32_t>(u0 - static_cast<int64_t>(rb) * a.n_sb) : 0;
-    const int32_t sb_end = (rb == rb_last) ? static_cast<int32_t>(u1 - static_cast<int64_t>(rb) * a.n_sb) : a.n_sb;
-#pragma unroll
-    for (int r = 0; r < kTaskSlots; ++r)
-#pragma unroll
-      for (int s = 0; s < kOut; ++s) acc[r][s] = 0ull;
-
-    for (int32_t sb = sb_begin; sb < sb_end; ++sb, ++i) {
-      const uint32_t full = bars + 8 * st;
-      bool ok = mbar_try_wait(full, ph);
-      if (!ok) {
-        ok = flag[0] == 0 && mbar_wait_bounded(full, ph, flags);
-        if (!ok && flag[0] == 0) {
-          atomicOr(&g_device_error, PTI_DEVERR_FULL_TIMEOUT);
-          flag[0] = 1;
-        }
-      }
-      if (ok) {
-        const uint8_t *tile = base_ptr + st * S::kBytes;
-        const uint8_t *xsb = tile + kStageBytes;
-        run_chunk<F, N>(pa, tile, xsb, lane, half, acc);
-        run_chunk<F, N>(pb, tile, xsb, lane, half, acc);
-        if (takes16 && (static_cast<uint32_t>(i) & 3u) == sched) run_chunk<F, N>(p16, tile, xsb, lane, half, acc);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + 8 * (stages + st));
-      if (++st == static_cast<uint32_t>(stages)) {
-        st = 0;
-        ph ^= 1u;
-      }
+  const ConsumerCtx cx{base_ptr, red, epi, flag, bars, flags, stages, tid, warp, lane, u0, u1};
+  auto release = [](int64_t, uint32_t, uint32_t) {};
+  if constexpr (F == Fmt::Q8) {
+    // Warp w always computes block b = w % 8 of every unit for the rows of half
+    // w / 8; the warps of a scheduler (w % 4) share the parity of b and so
+    // run one code body.
+    const uint32_t half = warp >> 3, blk = warp & 7u;
+    const uint32_t win_off = 32u * blk;
+    const bool c_hi = (blk & 4u) != 0u;
+    auto run = [&](auto ec, auto cc) {
+      constexpr int E_ = decltype(ec)::value;
+      constexpr int C_ = decltype(cc)::value;
+      consumer_loop<F, N, E>(a, cx, [&](const uint8_t *tile, const uint8_t *xsb, int64_t,
+                                        uint64_t (&acc)[kTaskSlots][kOut]) {
+        q8_block_body<N, E_, C_>(tile, xsb + 128u * blk, lane, half, win_off, c_hi, acc);
+      }, release);
+    };
+    switch (blk & 3u) {  // = warp % 4: one code body per scheduler
+      case 0: run(std::integral_constant<int, 0>{}, std::integral_constant<int, 0>{}); break;
+      case 1: run(std::integral_constant<int, 1>{}, std::integral_constant<int, 0>{}); break;
+      case 2: run(std::integral_constant<int, 0>{}, std::integral_constant<int, 1>{}); break;
+      default: run(std::integral_constant<int, 1>{}, std::integral_constant<int, 1>{}); break;
     }
-
-    // ---- park this warp's sums for the tile: slot 0 = first tile of the CTA,
-    //      slot 1 = any later one (only the last can be shared with another CTA)
-    const int sl = (rb == rb_first) ? 0 : 1;
-    const bool middle = rb != rb_first && rb != rb_last;
-#pragma unroll
-    for (int r = 0; r < kTaskSlots; ++r)
-#pragma unroll
-      for (int s = 0; s < kOut; ++s) {
-        const float2 v = unpack2(acc[r][s]);
-        red[((sl * kConsumerWarps + warp) * kOut + s) * 64 + r * 32 + lane] = v.x + v.y;
-      }
-    if (middle) {
-      // a tile wholly inside this CTA's range: finish it now (rare: only when
-      // a CTA spans more than two row tiles)
-      named_barrier(kBarConsumers, kConsumerThreads);
-      finish_tile<F, N, E>(a, red, 1, rb, tid, flag, epi);
-      named_barrier(kBarConsumers, kConsumerThreads);
-    }
-  }
-  named_barrier(kBarConsumers, kConsumerThreads);
-  finish_tile<F, N, E>(a, red, 0, rb_first, tid, flag, epi);
-  if (rb_last != rb_first) {
-    named_barrier(kBarConsumers, kConsumerThreads);
-    finish_tile<F, N, E>(a, red, 1, rb_last, tid, flag, epi);
+  } else {
+    // Twin: warp w runs on scheduler k = w % 4 and always works on the same two
+    // 16-byte chunks of every unit, rows of half j % 2 (j = w / 4): chunks
+    // k + 4(j/2) and k + 4(j/2) + 8, so each scheduler owns chunks k, k+4, k+8,
+    // k+12.  Chunk 16 of unit i goes to the warps j = 0, 1 of scheduler i % 4.
+    const uint32_t sched = warp & 3u, wj = warp >> 2;
+    const uint32_t half = wj & 1u;
+    const int ca = static_cast<int>(sched + 4u * (wj >> 1));
+    const ChunkParams pa = chunk_params<F, N>(ca), pb = chunk_params<F, N>(ca + 8), p16 = chunk_params<F, N>(16);
+    const bool takes16 = (wj >> 1) == 0u;
+    consumer_loop<F, N, E>(a, cx, [&](const uint8_t *tile, const uint8_t *xsb, int64_t i,
+                                      uint64_t (&acc)[kTaskSlots][kOut]) {
+      run_chunk<F, N>(pa, tile, xsb, lane, half, acc);
+      run_chunk<F, N>(pb, tile, xsb, lane, half, acc);
+      if (takes16 && (static_cast<uint32_t>(i) & 3u) == sched) run_chunk<F, N>(p16, tile, xsb, lane, half, acc);
+    }, release);
   }
 }
 

@@ -151,3 +151,15 @@ def test_decode_pass_validation(L):
     assert _decode(L, x_out=GATE + (1 << 30) + 64) == 5         # x_out inside layer 1's gate matrix
     assert _decode(L, ws=UP) == 5                                # workspace overlaps a weight matrix
     assert _decode(L, ws=FAKE + (8 << 34) - 256) == 5           # workspace overlaps x_in
+
+
+def test_ex_entry_points_reject_unknown_flags(L):
+    """The _ex variants validate like the plain ones and reject unknown flag bits."""
+    args = (FAKE, 128, 512, 2, FAKE + (1 << 30), FAKE + (2 << 30), FAKE + (3 << 30), 1 << 24, None)
+    assert L.pti_q8_gemv_nstream_ex(*args, 2) == 8 and L.pti_q8_gemv_nstream_ex(*args, 0x80000000) == 8
+    assert L.pti_q8_gemv_nstream_ex(None, *args[1:], 1) == 1
+    assert L.pti_q8_gemv_nstream_ex(FAKE, 128, 48, *args[3:], 1) == 2
+    targs = (FAKE, 128, 512, FAKE + (1 << 30), FAKE + (1 << 30), FAKE + (2 << 30), FAKE + (2 << 30) + 4096,
+             FAKE + (3 << 30), 1 << 24, None)
+    assert L.pti_ssq_twin_gemv_ex(*targs, 4) == 8
+    assert L.pti_ssq_twin_gemv_ex(None, *targs[1:], 1) == 1

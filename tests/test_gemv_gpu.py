@@ -154,6 +154,26 @@ def test_q8_streams_are_independent_at_full_size(full_q8):
         assert np.all(np.abs(y4[s, idx].astype(np.float64) - y1[0, idx]) <= 2 * TOL * bound[0])
 
 
+def test_q8_pdl_chain_reads_each_finished_output(full_q8):
+    """y1 = W1 x, then y2 = W2 y1 and y3 = W1 y2 launched with FLAG_PDL: each
+    may start while its predecessor still runs (prefetching weights), yet must
+    read the predecessor's finished output and share its workspace safely."""
+    a, b = full_q8[(17408, 5120)], full_q8[(5120, 17408)]
+    wa, wb = dev(a), dev(b)
+    x = dev(pti_synth.activations(4, 5120, seed=9))
+    y1 = pti.q8_gemv_nstream(wa, 17408, 5120, x)
+    y2 = pti.q8_gemv_nstream(wb, 5120, 17408, y1, flags=pti.FLAG_PDL)
+    y3 = pti.q8_gemv_nstream(wa, 17408, 5120, y2, flags=pti.FLAG_PDL)
+    torch.cuda.synchronize()
+    y1n, y2n, y3n = y1.cpu().numpy(), y2.cpu().numpy(), y3.cpu().numpy()
+    idx2 = tile_sample_rows(5120, np.random.default_rng(2))
+    r2, b2 = oracle.q8_gemv(b, 5120, 17408, y1n, rows_idx=idx2)
+    assert_parity(y2n[:, idx2], r2, b2, "pdl chain step 2")
+    idx3 = tile_sample_rows(17408, np.random.default_rng(3))
+    r3, b3 = oracle.q8_gemv(a, 17408, 5120, y2n, rows_idx=idx3)
+    assert_parity(y3n[:, idx3], r3, b3, "pdl chain step 3")
+
+
 # ---------------------------------------------------------------------------
 # SSQ twin GEMV
 # ---------------------------------------------------------------------------
@@ -206,6 +226,20 @@ def test_twin_full_size_matches_oracle_on_every_tile(full_twin, rows, cols):
     ya_ref, yb_ref, ba, bb = oracle.twin_gemv(w_np, rows, cols, xa, xb, rows_idx=idx)
     assert_parity(ya.cpu().numpy()[idx], ya_ref, ba, "twin A full")
     assert_parity(yb.cpu().numpy()[idx], yb_ref, bb, "twin B full")
+
+
+def test_twin_pdl_chain_reads_each_finished_output(full_twin):
+    """(y_A, y_B) of a 17408 x 5120 twin GEMV feed a 5120 x 17408 twin GEMV
+    launched with FLAG_PDL."""
+    a, b = full_twin[(17408, 5120)], full_twin[(5120, 17408)]
+    xa, xb = pti_synth.activations(2, 5120, seed=0, tensor_id=300)
+    ya, yb = pti.ssq_twin_gemv(dev(a), 17408, 5120, dev(xa), dev(xb))
+    za, zb = pti.ssq_twin_gemv(dev(b), 5120, 17408, ya, yb, flags=pti.FLAG_PDL)
+    torch.cuda.synchronize()
+    idx = tile_sample_rows(5120, np.random.default_rng(4))
+    ra, rb, ba, bb = oracle.twin_gemv(b, 5120, 17408, ya.cpu().numpy(), yb.cpu().numpy(), rows_idx=idx)
+    assert_parity(za.cpu().numpy()[idx], ra, ba, "twin pdl chain A")
+    assert_parity(zb.cpu().numpy()[idx], rb, bb, "twin pdl chain B")
 
 
 @pytest.mark.parametrize("rows,cols", [(17408, 5120), (5120, 17408)])
