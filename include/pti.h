@@ -221,7 +221,7 @@ pti_status pti_verify_greedy(const float *logits, const int32_t *guess,
  *              w_down[l] ([hidden][ffn/32] Q8 blocks), each 16-byte aligned.
  *              The arrays are read during the call only; layers may share
  *              matrices.
- *   n_layers   >= 1.
+ *   n_layers   1 .. 4096.
  *   hidden, ffn  multiples of 256, hidden * ffn < 2^40.
  *   n_streams  1..4.
  *   eps        finite, >= 0 (else PTI_ERR_VALUE).
@@ -236,15 +236,14 @@ pti_status pti_verify_greedy(const float *logits, const int32_t *guess,
  *              them before it ends, so every call that completes leaves the
  *              workspace zero-filled (one workspace may serve this call and the
  *              GEMVs above, ordered in one stream).
- * Work: 2 n_layers + 1 kernels.  Per layer, one kernel streams W_gate and W_up
- * together (64 gate rows and their 64 up rows per tile) and writes
- * SiLU(g) * u; one kernel streams W_down and applies h's RMS scale to its
- * output; each writes per-tile sums of squares of its output, from which the
- * next kernel takes the RMS scale of its input (W (c v) = c (W v), so no
- * separate normalisation pass over the vectors is needed).  A last kernel
- * applies the final RMS scale.  Kernels after the first start early
- * (programmatic dependent launch) and prefetch weights while the previous
- * one finishes; the first waits for all earlier work in the stream.
+ * Work per layer: a gate/up step streams W_gate and W_up together (64 gate
+ * rows and their 64 up rows per tile) and writes SiLU(g) * u; a down step
+ * streams W_down and applies h's RMS scale to its output; each writes per-tile
+ * sums of squares of its output, from which the next step takes the RMS scale
+ * of its input (W (c v) = c (W v), so no separate normalisation pass over the
+ * vectors is needed).  A last kernel applies the final RMS scale.  How the
+ * steps are launched: see pti_mlp_decode_pass_ex.  The first launch waits for
+ * all earlier work in the stream.
  * Arithmetic: GEMVs as in the conventions, SiLU with expf, RMS scales in
  * double from fp32 per-tile sums of squares; bit-reproducible run to run.
  */
@@ -255,6 +254,28 @@ pti_status pti_mlp_decode_pass(const void *const *w_gate, const void *const *w_u
                                const float *x_in, float *x_out,
                                void *workspace, size_t workspace_bytes,
                                pti_stream_t stream);
+
+/*
+ * pti_mlp_decode_pass with flags.  By default (flags 0) each gate/up and down
+ * step is its own launch, 2 n_layers + 1 launches chained by programmatic
+ * dependent launch.
+ *   PTI_FLAG_DECODE_PERSISTENT  run the steps in persistent cooperative
+ *                launches of up to 64 layers each instead (one CTA per SM, a
+ *                grid barrier between steps, the next step's weights streamed
+ *                in while the grid crosses the barrier), then the final
+ *                kernel; if the device cannot run a cooperative grid of one
+ *                CTA per SM the call returns PTI_ERR_CUDA and enqueues
+ *                nothing.
+ * Other flag bits return PTI_ERR_VALUE.  Same arguments and results
+ * otherwise; the two forms differ only in rounding order.
+ */
+#define PTI_FLAG_DECODE_PERSISTENT 0x2u
+
+pti_status pti_mlp_decode_pass_ex(const void *const *w_gate, const void *const *w_up, const void *const *w_down,
+                                  int n_layers, int64_t hidden, int64_t ffn, int n_streams, double eps,
+                                  const float *x_in, float *x_out,
+                                  void *workspace, size_t workspace_bytes,
+                                  pti_stream_t stream, uint32_t flags);
 
 /*
  * Reads and clears the device error word of the current device (a blocking

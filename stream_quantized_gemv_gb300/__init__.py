@@ -83,6 +83,9 @@ def lib() -> ctypes.CDLL:
             L.pti_mlp_decode_pass_workspace_bytes.argtypes = [I64, I64, I]
             L.pti_mlp_decode_pass.restype = I
             L.pti_mlp_decode_pass.argtypes = [P, P, P, I, I64, I64, I, ctypes.c_double, P, P, P, SZ, P]
+            L.pti_mlp_decode_pass_ex.restype = I
+            L.pti_mlp_decode_pass_ex.argtypes = [P, P, P, I, I64, I64, I, ctypes.c_double, P, P, P, SZ, P,
+                                                 ctypes.c_uint32]
             L.pti_device_error.restype = I
             L.pti_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             _lib = L
@@ -223,9 +226,15 @@ class DecodeWeights:
         self.n_layers = len(w_gate)
 
 
-def mlp_decode_pass(weights, hidden: int, ffn: int, x, eps: float = 1e-6, x_out=None, ws=None, stream=None):
+FLAG_DECODE_PERSISTENT = 0x2
+
+
+def mlp_decode_pass(weights, hidden: int, ffn: int, x, eps: float = 1e-6, x_out=None, ws=None, stream=None,
+                    persistent: bool = False):
     """Runs the gated-MLP layers of ``weights`` (a ``DecodeWeights``) over the
-    streams x [n][hidden] and returns x_out [n][hidden]."""
+    streams x [n][hidden] and returns x_out [n][hidden].  ``persistent`` runs
+    the steps in one cooperative launch per 64 layers instead of one launch
+    per step."""
     import torch
     if x.dim() == 1:
         x = x.unsqueeze(0)
@@ -235,10 +244,10 @@ def mlp_decode_pass(weights, hidden: int, ffn: int, x, eps: float = 1e-6, x_out=
     need = mlp_decode_pass_workspace_bytes(hidden, ffn, n)
     if ws is None:
         ws = workspace(need, x.device)
-    _check(lib().pti_mlp_decode_pass(weights.gate, weights.up, weights.down, weights.n_layers, hidden, ffn, n,
-                                     float(eps), _ptr(x), _ptr(x_out), _ptr(ws),
-                                     0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
-           "pti_mlp_decode_pass")
+    _check(lib().pti_mlp_decode_pass_ex(weights.gate, weights.up, weights.down, weights.n_layers, hidden, ffn, n,
+                                        float(eps), _ptr(x), _ptr(x_out), _ptr(ws),
+                                        0 if ws is None else ws.numel() * ws.element_size(), _stream(stream),
+                                        FLAG_DECODE_PERSISTENT if persistent else 0), "pti_mlp_decode_pass")
     return x_out
 
 

@@ -433,9 +433,11 @@ template <int kOut>
 __device__ __noinline__ void input_scales(const GemvArgs &a, uint32_t warp, uint32_t lane, float *scale) {
   if (warp >= static_cast<uint32_t>(kOut)) return;
   double s2 = 0.0;
-  if (a.sq_in != nullptr)
+  if (a.sq_in != nullptr) {
+#pragma unroll 4
     for (int32_t t = static_cast<int32_t>(lane); t < a.n_sq_in; t += 32)
       s2 += static_cast<double>(__ldcg(a.sq_in + static_cast<int64_t>(t) * kOut + warp));
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xFFFFFFFFu, s2, o);
   if (lane == 0) scale[warp] = a.sq_in != nullptr ? static_cast<float>(1.0 / sqrt(s2 * a.inv_len_in + a.eps)) : 1.0f;
@@ -737,21 +739,40 @@ struct Producer {
     }
   }
   // Weights do not depend on the previous kernel in the stream: fetch the
-  // first tiles before waiting for it, then their activations.
+  // first tiles before waiting for it, then their activations.  When the
+  // consumers are the slower side (Q8 with N >= 2), only kRamp stages go out
+  // at once and each further initial stage waits until the one kRamp before
+  // it has landed: with every SM requesting its whole ring at the same moment
+  // the first stage would otherwise land only after most of the burst
+  // (measured: about 4 us), and compute could not start before.
   __device__ __forceinline__ void start() {
     prefetch_tmap(tmap);
     if constexpr (E == Epi::GateUp) prefetch_tmap(tmap2);
+    constexpr int64_t kRamp = (F == Fmt::Q8 && N >= 2) ? 2 : kMaxStages;
     const int64_t pre = nu < stages ? nu : stages;
-    for (int64_t i = 0; i < pre; ++i) {
+    const int64_t first = pre < kRamp ? pre : kRamp;
+    for (int64_t i = 0; i < first; ++i) {
       mbar_expect_tx(bars + 8 * i, kStageBytes);
       load_w(i, static_cast<uint32_t>(i));
     }
     pdl_wait_primary();
-    for (int64_t i = 0; i < pre; ++i) {
+    for (int64_t i = 0; i < first; ++i) {
       mbar_arrive_expect_tx(bars + 8 * i, S::kXBytes);
       load_x(i, static_cast<uint32_t>(i));
     }
-    issued = pre;
+    issued = first;
+    for (int64_t i = first; i < pre; ++i) {
+      const uint32_t landed = bars + 8 * static_cast<uint32_t>(i - kRamp);
+      if (!mbar_try_wait(landed, 0) && !mbar_wait_bounded(landed, 0, flags)) {
+        if (flag[0] == 0) atomicOr(&g_device_error, PTI_DEVERR_FULL_TIMEOUT);
+        flag[0] = 1;
+        return;
+      }
+      mbar_arrive_expect_tx(bars + 8 * i, kStageBytes + S::kXBytes);
+      load_w(i, static_cast<uint32_t>(i));
+      load_x(i, static_cast<uint32_t>(i));
+      issued = i + 1;
+    }
   }
   // Once every consumer warp has released unit i (ring slot st, phase parity
   // ph), fetch unit i + stages into the slot.

@@ -163,3 +163,13 @@ def test_ex_entry_points_reject_unknown_flags(L):
              FAKE + (3 << 30), 1 << 24, None)
     assert L.pti_ssq_twin_gemv_ex(*targs, 4) == 8
     assert L.pti_ssq_twin_gemv_ex(None, *targs[1:], 1) == 1
+
+
+def test_decode_pass_ex_rejects_unknown_flags(L):
+    ok_bytes = L.pti_mlp_decode_pass_workspace_bytes(512, 1024, 4)
+    gate, up, down = _ptrs(GATE), _ptrs(UP), _ptrs(DOWN)
+    args = (gate, up, down, 1, 512, 1024, 4, 1e-6, FAKE + (8 << 34), FAKE + (9 << 34), FAKE + (10 << 34),
+            ok_bytes, None)
+    assert L.pti_mlp_decode_pass_ex(*args, 1) == 8 and L.pti_mlp_decode_pass_ex(*args, 4) == 8
+    assert L.pti_mlp_decode_pass_ex(gate, up, down, 0, *args[4:], 2) == 2
+    assert L.pti_mlp_decode_pass_ex(gate, up, down, 4097, *args[4:], 0) == 2

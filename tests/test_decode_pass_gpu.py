@@ -92,22 +92,22 @@ def check_layer(got, xo, tol, what):
         raise AssertionError(f"{what}: {(err > tol).sum()} outputs off; worst {i}: err {err[i]:.3g}, bar {tol[i]:.3g}")
 
 
-def run_pass(weights, n_layers, hidden, ffn, x, eps=EPS):
+def run_pass(weights, n_layers, hidden, ffn, x, eps=EPS, persistent=False):
     w = pti.DecodeWeights(weights.tensors[0][:n_layers], weights.tensors[1][:n_layers],
                           weights.tensors[2][:n_layers])
-    y = pti.mlp_decode_pass(w, hidden, ffn, x, eps=eps)
+    y = pti.mlp_decode_pass(w, hidden, ffn, x, eps=eps, persistent=persistent)
     torch.cuda.synchronize()
     return y.cpu().numpy()
 
 
-def check_chain(layers, hidden, ffn, n, seed, eps=EPS, x=None):
+def check_chain(layers, hidden, ffn, n, seed, eps=EPS, x=None, persistent=False):
     w = device_weights(layers)
     if x is None:
         x = pti_synth.activations(n, hidden, seed, 1000)
     xd = dev(x)
     prev = x.astype(np.float64)
     for k in range(1, len(layers) + 1):
-        got = run_pass(w, k, hidden, ffn, xd, eps)
+        got = run_pass(w, k, hidden, ffn, xd, eps, persistent)
         xo, tol = layer_tolerance(*layers[k - 1], hidden, ffn, prev.astype(np.float32), eps)
         check_layer(got, xo, tol, f"hidden {hidden} ffn {ffn} n {n} layer {k}")
         prev = got.astype(np.float64)
@@ -117,18 +117,35 @@ def check_chain(layers, hidden, ffn, n, seed, eps=EPS, x=None):
 # shapes: stream-K tiles shared by several CTAs (256x512, 768x1280), whole
 # tiles per CTA in the down kernel (4096x256), CTAs spanning more than two
 # gate/up tiles (256x40960)
+@pytest.mark.parametrize("persistent", [False, True])
 @pytest.mark.parametrize("hidden,ffn", [(256, 512), (768, 1280), (4096, 256), (256, 40960)])
 @pytest.mark.parametrize("n", [1, 2, 3, 4])
-def test_decode_pass_one_layer(hidden, ffn, n):
+def test_decode_pass_one_layer(hidden, ffn, n, persistent):
     layers = host_layers(1, hidden, ffn, seed=hidden + ffn)
-    check_chain(layers, hidden, ffn, n, seed=n)
+    check_chain(layers, hidden, ffn, n, seed=n, persistent=persistent)
 
 
+@pytest.mark.parametrize("persistent", [False, True])
 @pytest.mark.parametrize("n", [1, 4])
-def test_decode_pass_three_layers(n):
+def test_decode_pass_three_layers(n, persistent):
     hidden, ffn = 512, 1536
     layers = host_layers(3, hidden, ffn, seed=5)
-    check_chain(layers, hidden, ffn, n, seed=7)
+    check_chain(layers, hidden, ffn, n, seed=7, persistent=persistent)
+
+
+def test_decode_pass_more_layers_than_one_launch_holds():
+    """70 layers: the persistent form splits them over two launches (64 + 6);
+    the layers on both sides of the launch boundary and the last one stay
+    within their bars."""
+    hidden, ffn, n = 256, 512, 2
+    layers = host_layers(70, hidden, ffn, seed=31)
+    x = pti_synth.activations(n, hidden, 31, 1000)
+    w = device_weights(layers)
+    for k in (64, 65, 70):
+        g_k = run_pass(w, k, hidden, ffn, dev(x), persistent=True)
+        g_prev = run_pass(w, k - 1, hidden, ffn, dev(x), persistent=True)
+        xo, tol = layer_tolerance(*layers[k - 1], hidden, ffn, g_prev.astype(np.float32))
+        check_layer(g_k, xo, tol, f"persistent layer {k}")
 
 
 def test_decode_pass_eps_matters():
@@ -209,12 +226,14 @@ def test_decode_pass_full_size_two_layers():
                           [d for _, _, d in layers_dev])
     x = pti_synth.activations(n, hidden, 0, 1000)
     xd = dev(x)
-    prev = x.astype(np.float64)
-    for k in (1, 2):
-        got = run_pass(w, k, hidden, ffn, xd)
-        g, u, d = (t.cpu().numpy() for t in layers_dev[k - 1])
-        xo, tol = layer_tolerance(g, u, d, hidden, ffn, prev.astype(np.float32))
-        check_layer(got, xo, tol, f"full size layer {k}")
-        prev = got.astype(np.float64)
+    g, u, d = (t.cpu().numpy() for t in layers_dev[0])
+    got1 = run_pass(w, 1, hidden, ffn, xd)
+    xo, tol = layer_tolerance(g, u, d, hidden, ffn, x)
+    check_layer(got1, xo, tol, "full size layer 1")
+    g, u, d = (t.cpu().numpy() for t in layers_dev[1])
+    xo, tol = layer_tolerance(g, u, d, hidden, ffn, got1.astype(np.float32))
+    for persistent in (False, True):
+        got2 = run_pass(w, 2, hidden, ffn, xd, persistent=persistent)
+        check_layer(got2, xo, tol, f"full size layer 2 persistent={persistent}")
     del layers_dev, w
     torch.cuda.empty_cache()
