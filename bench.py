@@ -188,10 +188,14 @@ class Q8Pass:
         self.dtype = "f32"
 
     def step(self, x=None, y=None):
+        # a chain of GEMVs as in a decode step: every launch after the first
+        # may start while the previous one finishes (programmatic dependent
+        # launch; the weights are never written)
         x = self.x if x is None else x
         y = self.y if y is None else y
-        for w in self.w:
-            self.pti.q8_gemv_nstream(w, self.rows, self.cols, x, y=y, ws=self.ws)
+        for k, w in enumerate(self.w):
+            self.pti.q8_gemv_nstream(w, self.rows, self.cols, x, y=y, ws=self.ws,
+                                     flags=self.pti.FLAG_PDL if k > 0 else 0)
 
     def e2e_buffers(self):
         t = self.torch
@@ -202,7 +206,8 @@ class Q8Pass:
 
     def config(self):
         return {"workload": f"N-stream Q8 GEMV weight pass: {self.layers} distinct {self.rows}x{self.cols} "
-                            f"Q8 matrices (f16 scale + 32 int8 per 34-byte block), N={self.n} fp32 streams",
+                            f"Q8 matrices (f16 scale + 32 int8 per 34-byte block), N={self.n} fp32 streams, "
+                            "launches after the first with programmatic dependent launch",
                 "rows": self.rows, "cols": self.cols, "n_streams": self.n, "matrices_per_step": self.layers,
                 "weight_bytes_per_step": self.layers * self.weight_bytes,
                 "l2": f"inputs larger than L2: {self.layers * self.weight_bytes / 1e9:.2f} GB of distinct "
@@ -245,8 +250,9 @@ class TwinPass(Q8Pass):
     def step(self, x=None, y=None):
         x = self.x if x is None else x
         y = self.y if y is None else y
-        for w in self.w:
-            self.pti.ssq_twin_gemv(w, self.rows, self.cols, x[0], x[1], y_a=y[0], y_b=y[1], ws=self.ws)
+        for k, w in enumerate(self.w):
+            self.pti.ssq_twin_gemv(w, self.rows, self.cols, x[0], x[1], y_a=y[0], y_b=y[1], ws=self.ws,
+                                   flags=self.pti.FLAG_PDL if k > 0 else 0)
 
     def config(self):
         return {"workload": f"SSQ mode-16 twin GEMV: {self.layers} distinct {self.rows}x{self.cols} twin "

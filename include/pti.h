@@ -89,15 +89,18 @@ const char *pti_status_string(pti_status status);
  *   y          [n_streams][rows] fp32 out, 4-byte aligned, overlapping neither
  *              w_q8 nor x.
  *   workspace  device scratch of at least pti_q8_gemv_workspace_bytes(rows,
- *              cols, n_streams) bytes, 256-byte aligned, zero-filled before its
- *              first use (every call that completes leaves all of it zero-filled
- *              again, so one workspace serves calls of any shape and stream
- *              count);
- *              may be NULL when that size is 0.  Calls that share a workspace
- *              must be ordered (same stream or synchronised).
+ *              cols, n_streams) bytes (at most 1,310,720 bytes: it depends only
+ *              on n_streams), 256-byte aligned; its contents need no
+ *              initialisation and are undefined afterwards, so one workspace
+ *              serves calls of any shape and stream count; may be NULL when
+ *              that size is 0.  Calls that share a workspace must be ordered
+ *              (same stream or synchronised).
  * Fast path when cols % 256 == 0 and x is 16-byte aligned: TMA-streamed,
- * persistent, one pass over the weights; other calls use a plain per-row
- * kernel with the same bound on the error (a different rounding order).
+ * persistent, one pass over the weights, followed by a small kernel that
+ * adds the partial sums of the row tiles several CTAs shared (launched with
+ * programmatic dependent launch, so it waits for the GEMV without a launch
+ * gap); other calls use a plain per-row kernel with the same bound on the
+ * error (a different rounding order).
  */
 size_t pti_q8_gemv_workspace_bytes(int64_t rows, int64_t cols, int n_streams);
 
@@ -136,16 +139,13 @@ pti_status pti_q8_gemv_nstream_ex(const void *w_q8, int64_t rows, int64_t cols, 
  * Same arguments, results and checks as pti_q8_gemv_nstream, without the
  * workspace: the scratch it needs lives in a 2 MiB array inside this library
  * (pti_q8_gemv_noalloc_max_scratch_bytes()), held by every GPU that loads the
- * library until the process exits.  It serves any shape whose workspace fits,
- * i.e. up to 25,165,824 rows at n_streams = 4 (56,623,104 at n_streams = 1) on
- * the cols % 256 == 0 path; larger requests return PTI_ERR_WORKSPACE before
- * anything is enqueued.  The call allocates nothing.
+ * library until the process exits.  Every valid shape fits (the scratch
+ * depends only on n_streams, at most 1.31 MB); a request for more would return
+ * PTI_ERR_WORKSPACE before anything is enqueued.  The call allocates nothing.
  *
- * The first call on a device sets the array up (looks up its device address,
- * zero-fills it and synchronises the device); make that first call before any
- * stream capture.  All calls on a device share the one array, which keeps the
- * last call's contents (every completed call leaves it zero-filled): calls
- * that overlap on the GPU race, so order them (one stream, or synchronise).
+ * The first call on a device looks up the array's device address.  All calls
+ * on a device share the one array: calls that overlap on the GPU race, so
+ * order them (one stream, or synchronise).
  */
 size_t pti_q8_gemv_noalloc_max_scratch_bytes(void);
 
@@ -162,7 +162,8 @@ pti_status pti_q8_gemv_nstream_noalloc(const void *w_q8, int64_t rows, int64_t c
  *   rows, cols as for the Q8 GEMV.
  *   x_a, x_b   [cols] fp32 (A's and B's activations; may be the same pointer).
  *   y_a, y_b   [rows] fp32 out; distinct, overlapping no input.
- *   workspace  as for the Q8 GEMV, sized by pti_ssq_twin_gemv_workspace_bytes.
+ *   workspace  as for the Q8 GEMV (scratch, no initialisation), sized by
+ *              pti_ssq_twin_gemv_workspace_bytes.
  * Fast path when cols % 128 == 0 and x_a, x_b are 16-byte aligned.
  */
 size_t pti_ssq_twin_gemv_workspace_bytes(int64_t rows, int64_t cols);
@@ -230,12 +231,11 @@ pti_status pti_verify_greedy(const float *logits, const int32_t *guess,
  *   x_out      [n_streams][hidden] fp32 out, 4-byte aligned, overlapping no
  *              weight matrix; may be x_in (in place).
  *   workspace  at least pti_mlp_decode_pass_workspace_bytes(hidden, ffn,
- *              n_streams) bytes, 256-byte aligned, overlapping no argument,
- *              zero-filled before its first use.  The pass keeps h, each
- *              layer's output and per-tile sums of squares there and clears
- *              them before it ends, so every call that completes leaves the
- *              workspace zero-filled (one workspace may serve this call and the
- *              GEMVs above, ordered in one stream).
+ *              n_streams) bytes, 256-byte aligned, overlapping no argument;
+ *              scratch (h, each layer's raw output, per-tile sums of squares,
+ *              partial sums): no initialisation needed, contents undefined
+ *              afterwards.  One workspace may serve this call and the GEMVs
+ *              above, ordered in one stream.
  * Work per layer: a gate/up step streams W_gate and W_up together (64 gate
  * rows and their 64 up rows per tile) and writes SiLU(g) * u; a down step
  * streams W_down and applies h's RMS scale to its output; each writes per-tile

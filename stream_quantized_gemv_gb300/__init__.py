@@ -112,8 +112,8 @@ _ws_cache: dict = {}
 
 
 def workspace(nbytes: int, device):
-    """A zero-filled device buffer of at least ``nbytes`` bytes, reused across
-    calls on the same device (every completed call leaves it zero-filled)."""
+    """A device scratch buffer of at least ``nbytes`` bytes, reused across calls
+    on the same device (the library needs no initialisation of it)."""
     import torch
     if nbytes == 0:
         return None

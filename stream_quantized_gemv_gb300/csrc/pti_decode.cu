@@ -17,8 +17,9 @@
 //                   per-tile sums of h^2 -> sq_h.
 //   kernel Down:    x'' = a (W_down h) with a = 1 / sqrt(sum(sq_h)/ffn + eps),
 //                   per-tile sums of x''^2 -> sq_x.
-// then one finalise kernel: x_out = b x'' (b from sq_x), and the scratch is
-// zeroed.  Every kernel after the first is launched with programmatic
+// then one finalise kernel: x_out = b x'' (b from sq_x).  After each GEMV a
+// small kernel combines the row tiles that several CTAs shared.  Every kernel
+// after the first is launched with programmatic
 // dependent launch; each waits for its predecessor to complete before it reads
 // anything but weights or writes anything, so one buffer of each kind serves
 // every layer.
@@ -79,21 +80,15 @@ pti_status check_decode_shape(int64_t hidden, int64_t ffn) {
 }
 
 struct FinalizeArgs {
-  float *xraw;              // [n][hidden] the last layer's raw output; zeroed
-  float *h;                 // [n][ffn] zeroed
-  float *sq_h;              // [n_rb_gu][n] zeroed
-  float *sq_x;              // [n_rb_down][n] read, then zeroed by the last CTA
-  unsigned int *counter;    // CTA arrival counter (zero between calls)
-  unsigned int *grid_bars;  // [n_grid_bars] grid-barrier counters of the persistent pass, zeroed
-  int32_t n_grid_bars;
+  const float *xraw;        // [n][hidden] the last layer's raw output
+  const float *sq_x;        // [n_rb_down][n] its per-tile sums of squares
   float *x_out;             // [n][hidden]
-  int64_t hidden, ffn;
-  int32_t n_rb_gu, n_rb_down;
+  int64_t hidden;
+  int32_t n_rb_down;
   double inv_hidden, eps;
 };
 
-// x_out = b x'' with b the RMS scale of the last layer's output, then zeroes
-// the pass's scratch so the workspace is all zero when the call completes.
+// x_out = b x'' with b the RMS scale of the last layer's output.
 template <int N>
 __global__ void __launch_bounds__(kFinalizeThreads) rms_finalize_kernel(const FinalizeArgs f) {
   __shared__ float scale[4];
@@ -114,18 +109,6 @@ __global__ void __launch_bounds__(kFinalizeThreads) rms_finalize_kernel(const Fi
   for (int64_t i = first; i < N * f.hidden; i += stride) {
     const int s = static_cast<int>(i / f.hidden);
     f.x_out[i] = __ldcg(f.xraw + i) * scale[s];
-    f.xraw[i] = 0.0f;
-  }
-  for (int64_t i = first; i < N * f.ffn; i += stride) f.h[i] = 0.0f;
-  for (int64_t i = first; i < static_cast<int64_t>(N) * f.n_rb_gu; i += stride) f.sq_h[i] = 0.0f;
-  for (int64_t i = first; i < f.n_grid_bars; i += stride) f.grid_bars[i] = 0u;
-  __syncthreads();  // this CTA's reads of sq_x are done
-  if (tid == 0) {
-    const unsigned int prev = atomicAdd(f.counter, 1u);
-    if (prev == gridDim.x - 1) {  // every CTA has read sq_x
-      for (int64_t i = 0; i < static_cast<int64_t>(N) * f.n_rb_down; ++i) f.sq_x[i] = 0.0f;
-      *f.counter = 0u;
-    }
   }
 }
 
@@ -408,6 +391,7 @@ __global__ void __launch_bounds__(kWarpCount * 32 + 32, 1)
       a.y0 = ph.y0;
       a.part = P.part;
       a.tickets = P.tickets;
+      a.combine_in_kernel = 1;
       a.rows = ph.rows;
       a.cols = ph.cols;
       a.units = ph.units;
@@ -494,26 +478,19 @@ __global__ void __launch_bounds__(kWarpCount * 32 + 32, 1)
 
 // Final kernel of a pass: applies the last RMS scale and zeroes the scratch.
 template <int N>
-pti_status launch_finalize(const DecodeLayout &d, uint8_t *ws, int64_t hidden, int64_t ffn, double eps, float *x_out,
-                           int n_grid_bars, cudaStream_t stream) {
+pti_status launch_finalize(const DecodeLayout &d, uint8_t *ws, int64_t hidden, double eps, float *x_out,
+                           cudaStream_t stream) {
   FinalizeArgs f;
-  f.xraw = reinterpret_cast<float *>(ws + d.xraw);
-  f.h = reinterpret_cast<float *>(ws + d.h);
-  f.sq_h = reinterpret_cast<float *>(ws + d.sq_h);
-  f.sq_x = reinterpret_cast<float *>(ws + d.sq_x);
-  f.counter = reinterpret_cast<unsigned int *>(ws + d.counter);
-  f.grid_bars = reinterpret_cast<unsigned int *>(ws + d.grid_bars);
-  f.n_grid_bars = n_grid_bars;
+  f.xraw = reinterpret_cast<const float *>(ws + d.xraw);
+  f.sq_x = reinterpret_cast<const float *>(ws + d.sq_x);
   f.x_out = x_out;
   f.hidden = hidden;
-  f.ffn = ffn;
-  f.n_rb_gu = static_cast<int32_t>(d.n_rb_gu);
   f.n_rb_down = static_cast<int32_t>(d.n_rb_down);
   f.inv_hidden = 1.0 / static_cast<double>(hidden);
   f.eps = eps;
   const int sms = current_device_sms();
   if (sms <= 0) return PTI_ERR_CUDA;
-  const int64_t blocks = std::min<int64_t>(sms, (static_cast<int64_t>(N) * ffn + kFinalizeThreads - 1) / kFinalizeThreads);
+  const int64_t blocks = std::min<int64_t>(sms, (static_cast<int64_t>(N) * hidden + kFinalizeThreads - 1) / kFinalizeThreads);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(kFinalizeThreads);
@@ -568,7 +545,7 @@ pti_status run_decode_chained(const void *const *w_gate, const void *const *w_up
     if (const pti_status s = launch_gemv<Fmt::Q8, N, Epi::Down>(w_down[l], nullptr, dn, stream, true); s != PTI_OK)
       return s;
   }
-  return launch_finalize<N>(d, ws, hidden, ffn, eps, x_out, 0, stream);
+  return launch_finalize<N>(d, ws, hidden, eps, x_out, stream);
 }
 
 // Shared memory of the persistent kernel: the ring, the parked warp sums,
@@ -615,6 +592,8 @@ pti_status run_decode_persistent(const void *const *w_gate, const void *const *w
   const int32_t grid = static_cast<int32_t>(std::min<int64_t>({static_cast<int64_t>(sms), units_gu, units_dn,
                                                                static_cast<int64_t>(kMaxGrid)}));
   const int n_launch = (n_layers + kMaxLayersPerLaunch - 1) / kMaxLayersPerLaunch;
+  // the in-kernel tile tickets and the grid-barrier counters start at zero
+  if (cudaMemsetAsync(ws + d.tickets, 0, d.h - d.tickets, stream) != cudaSuccess) return launch_status();
   static thread_local DecodeKernelParams P;  // about 25 KB: kept off the stack
   for (int c = 0; c < n_launch; ++c) {
     const int l0 = c * kMaxLayersPerLaunch;
@@ -653,7 +632,7 @@ pti_status run_decode_persistent(const void *const *w_gate, const void *const *w
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, decode_pass_kernel<N>, P) != cudaSuccess) return launch_status();
   }
-  return launch_finalize<N>(d, ws, hidden, ffn, eps, x_out, n_launch, stream);
+  return launch_finalize<N>(d, ws, hidden, eps, x_out, stream);
 }
 
 template <int N>

@@ -121,13 +121,13 @@ extern "C" const char *pti_status_string(pti_status status) {
 extern "C" size_t pti_q8_gemv_workspace_bytes(int64_t rows, int64_t cols, int n_streams) {
   if (check_gemv_shape(rows, cols) != PTI_OK || n_streams < 1 || n_streams > 4) return 0;
   if (cols % 256 != 0) return 0;
-  return fast_workspace_bytes<Fmt::Q8>(rows, n_streams);
+  return fast_workspace_bytes(n_streams);
 }
 
 extern "C" size_t pti_ssq_twin_gemv_workspace_bytes(int64_t rows, int64_t cols) {
   if (check_gemv_shape(rows, cols) != PTI_OK) return 0;
   if (cols % 128 != 0) return 0;
-  return fast_workspace_bytes<Fmt::Twin>(rows, 2);
+  return fast_workspace_bytes(2);
 }
 
 namespace {
@@ -246,9 +246,8 @@ constexpr size_t kNoAllocScratchBytes = size_t{2} << 20;  // 2 MiB per device
 static __device__ __align__(256) unsigned char g_pti_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
-// Device address of g_pti_noalloc_scratch on the current device.  The first
-// call on a device looks the address up (the array's name is only a host-side
-// stand-in), zero-fills the array and synchronises the device.
+// Device address of g_pti_noalloc_scratch on the current device (looked up
+// once per device; the array's name is only a host-side stand-in).
 pti_status noalloc_scratch_address(void **out) {
   static std::mutex mu;
   static void *addr[128] = {};
@@ -261,8 +260,6 @@ pti_status noalloc_scratch_address(void **out) {
   if (addr[dev] == nullptr) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_pti_noalloc_scratch) != cudaSuccess || p == nullptr) return launch_status();
-    if (cudaMemset(p, 0, kNoAllocScratchBytes) != cudaSuccess) return launch_status();
-    if (cudaDeviceSynchronize() != cudaSuccess) return launch_status();
     addr[dev] = p;
   }
   *out = addr[dev];
@@ -278,7 +275,7 @@ extern "C" pti_status pti_q8_gemv_nstream_noalloc(const void *w_q8, int64_t rows
   if (const pti_status st = check_gemv_shape(rows, cols); st != PTI_OK) return st;
   if (n_streams < 1 || n_streams > 4) return PTI_ERR_NSTREAMS;
   const size_t need = pti_q8_gemv_workspace_bytes(rows, cols, n_streams);
-  if (need > kNoAllocScratchBytes) return PTI_ERR_WORKSPACE;  // more rows than the built-in scratch serves
+  if (need > kNoAllocScratchBytes) return PTI_ERR_WORKSPACE;  // cannot happen for a valid shape today
   void *scratch = nullptr;
   if (need > 0) {
     if (const pti_status st = noalloc_scratch_address(&scratch); st != PTI_OK) return st;

@@ -124,7 +124,7 @@ struct GemvArgs {
   float *y0;        // Q8: y [N][rows]; twin: y_a
   float *y1;        // twin: y_b
   float *part;      // workspace: [grid][2 slots][kOut][128] partial sums
-  unsigned int *tickets;  // workspace: [n_rb] arrival counters (zero between calls)
+  unsigned int *tickets;  // in-kernel combining only: [n_rb] arrival counters, zero at start
   int64_t rows, cols, units;  // GateUp: rows = gate rows = up rows = outputs per stream
   int32_t n_sb, n_rb, grid, stages;
   // Fused epilogues only (Epi::GateUp, Epi::Down):
@@ -133,6 +133,7 @@ struct GemvArgs {
   double inv_len_in;   // 1 / length of each input vector
   double eps;          // added to the mean square before the square root
   int32_t n_sq_in;
+  int32_t combine_in_kernel;  // 1: tickets and the last CTA combine shared tiles; 0: combine_tiles_kernel does
 };
 
 // Rows handled by one warp task: lane l owns rows 64h + l and 64h + 32 + l of
@@ -503,14 +504,54 @@ __device__ __forceinline__ int red_warp(int q, int h) {
   else return (q >> 2) * 8 + h * 4 + (q & 3);
 }
 
+// Total of element (s, row) of shared tile rb: the partials of its CTAs
+// c_lo .. c_hi added in CTA order (each CTA's slot: 0 if rb is its first
+// tile, else 1), so the result does not depend on which CTA adds them.
+template <int kOut>
+__device__ __forceinline__ float sum_partials(const GemvArgs &a, int32_t rb, int32_t c_lo, int32_t c_hi, int s,
+                                              int row) {
+  float total = 0.0f;
+  for (int32_t c = c_lo; c <= c_hi; ++c) {
+    const int cs = (rb == first_tile_of_cta(c, a.units, a.grid, a.n_sb)) ? 0 : 1;
+    const float v = __ldcg(&a.part[((static_cast<int64_t>(c) * 2 + cs) * kOut + s) * kRowsPerTile + row]);
+    total = (c == c_lo) ? v : total + v;
+  }
+  return total;
+}
+
+// Writes element (s, row) of tile rb: y for Plain, else the epilogue's tile
+// buffer.
+template <Fmt F, int N, Epi E>
+__device__ __forceinline__ void deliver(const GemvArgs &a, float *tile_out, int32_t rb, int s, int row, float total) {
+  if constexpr (E == Epi::Plain) {
+    const int64_t row_g = static_cast<int64_t>(rb) * kRowsPerTile + row;
+    if (row_g < a.rows) {
+      if constexpr (F == Fmt::Q8) a.y0[s * a.rows + row_g] = total;
+      else (s == 0 ? a.y0 : a.y1)[row_g] = total;
+    }
+  } else {
+    tile_out[s * kRowsPerTile + row] = total;
+  }
+}
+
+template <int kOut, Epi E>
+__device__ __forceinline__ void run_epilogue(const GemvArgs &a, float *epi, int32_t rb, uint32_t tid,
+                                             uint32_t threads) {
+  float *const scale = epi + 4 * kRowsPerTile;
+  if constexpr (E == Epi::GateUp) gateup_epilogue<kOut>(a, epi, scale, scale + 4, rb, tid, threads);
+  else if constexpr (E == Epi::Down) down_epilogue<kOut>(a, epi, scale, scale + 4, rb, tid, threads);
+}
+
 // Finishes one or two row tiles of the CTA: tile k (row tile rb[k], deferred
 // warp sums in red slot sl[k]).  Each element's total is the tree sum of the 8
 // warps that computed it.  A tile no other CTA shares is written out directly
 // (Plain) or through the fused epilogue.  A shared tile's totals go to this
-// CTA's partial slot in the workspace; after one fence and one ticket per
-// tile (both tiles in the same round, so the round trips to L2 overlap), the
-// last CTA to arrive at a tile adds the partials of all its CTAs in CTA order
-// and writes the result; the others are done with it.
+// CTA's partial slot in the workspace.  With a.combine_in_kernel == 0 that is
+// all: a separate kernel (combine_tiles_kernel) adds the partials of every
+// shared tile once the GEMV has completed, so a CTA leaves the SM right after
+// its last tile.  Otherwise (the persistent decode pass, which has no kernel
+// boundary to wait on) one fence and one ticket per tile follow, both tiles
+// in the same round, and the last CTA to arrive at a tile adds its partials.
 // Not inlined: it runs a few times per CTA, and one shared copy keeps the
 // consumer loops' instruction footprint small.
 template <Fmt F, int N, Epi E>
@@ -519,9 +560,6 @@ __device__ __noinline__ void finish_tiles(const GemvArgs &a, const float *red, i
   using T = Traits<F, N>;
   constexpr int kOut = T::kOut;
   constexpr int kConsumerThreads = T::kWarps * 32;
-  float *const tile_out = epi;                  // [kOut][128]
-  float *const scale = epi + 4 * kRowsPerTile;  // [kOut]
-  float *const wsum = scale + 4;                // [16]
   const int32_t rbs[2] = {rb0, rb1};
   const int sls[2] = {sl0, sl1};
   int32_t clo[2] = {0, 0}, chi[2] = {0, 0};
@@ -538,36 +576,36 @@ __device__ __noinline__ void finish_tiles(const GemvArgs &a, const float *red, i
       v[q] = red[((sls[k] * T::kWarps + red_warp<F>(q, row >> 6)) * kOut + s) * 64 + (row & 63)];
     return tree_sum(v);
   };
-  auto part_slot = [&](int32_t cta, int slot, int s, int row) {
-    return &a.part[((static_cast<int64_t>(cta) * 2 + slot) * kOut + s) * kRowsPerTile + row];
-  };
-  // ---- shared tiles: publish this CTA's partials, one ticket round for all
+  // ---- shared tiles: publish this CTA's partials
   uint32_t last_bits = 0;
   if (any_shared) {
     for (int k = 0; k < count; ++k) {
       if (chi[k] == clo[k]) continue;
       for (int t = tid; t < kOut * kRowsPerTile; t += kConsumerThreads) {
         const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
-        *part_slot(static_cast<int32_t>(blockIdx.x), sls[k], s, row) = warp_total(k, s, row);
+        a.part[((static_cast<int64_t>(blockIdx.x) * 2 + sls[k]) * kOut + s) * kRowsPerTile + row] =
+            warp_total(k, s, row);
       }
     }
-    __threadfence();
-    named_barrier(kBarConsumers, kConsumerThreads);
-    if (tid == 0) {
-      uint32_t bits = 0;
-      for (int k = 0; k < count; ++k) {
-        if (chi[k] == clo[k]) continue;
-        const unsigned int prev = atomicAdd(&a.tickets[rbs[k]], 1u);
-        if (prev == static_cast<unsigned int>(chi[k] - clo[k])) {
-          a.tickets[rbs[k]] = 0u;  // leave the workspace zeroed for the next call
-          bits |= 1u << k;
+    if (a.combine_in_kernel) {
+      __threadfence();
+      named_barrier(kBarConsumers, kConsumerThreads);
+      if (tid == 0) {
+        uint32_t bits = 0;
+        for (int k = 0; k < count; ++k) {
+          if (chi[k] == clo[k]) continue;
+          const unsigned int prev = atomicAdd(&a.tickets[rbs[k]], 1u);
+          if (prev == static_cast<unsigned int>(chi[k] - clo[k])) {
+            a.tickets[rbs[k]] = 0u;  // ready for the next phase
+            bits |= 1u << k;
+          }
         }
+        if (bits != 0u) __threadfence();
+        flag[1] = bits;
       }
-      if (bits != 0u) __threadfence();
-      flag[1] = bits;
+      named_barrier(kBarConsumers, kConsumerThreads);
+      last_bits = flag[1];
     }
-    named_barrier(kBarConsumers, kConsumerThreads);
-    last_bits = flag[1];
   }
   // ---- write out the tiles this CTA completes
   bool epilogue_ran = false;
@@ -578,35 +616,43 @@ __device__ __noinline__ void finish_tiles(const GemvArgs &a, const float *red, i
       if (epilogue_ran) named_barrier(kBarConsumers, kConsumerThreads);  // tile_out and wsum are reused
     for (int t = tid; t < kOut * kRowsPerTile; t += kConsumerThreads) {
       const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
-      float total;
-      if (!shared_tile) {
-        total = warp_total(k, s, row);
-      } else {
-        total = 0.0f;
-        for (int32_t c = clo[k]; c <= chi[k]; ++c) {
-          const int cs = (rbs[k] == first_tile_of_cta(c, a.units, a.grid, a.n_sb)) ? 0 : 1;
-          float *const slot_ptr = part_slot(c, cs, s, row);
-          const float v = __ldcg(slot_ptr);
-          *slot_ptr = 0.0f;  // the whole workspace is zero again when the call completes
-          total = (c == clo[k]) ? v : total + v;
-        }
-      }
-      if constexpr (E == Epi::Plain) {
-        const int64_t row_g = static_cast<int64_t>(rbs[k]) * kRowsPerTile + row;
-        if (row_g < a.rows) {
-          if constexpr (F == Fmt::Q8) a.y0[s * a.rows + row_g] = total;
-          else (s == 0 ? a.y0 : a.y1)[row_g] = total;
-        }
-      } else {
-        tile_out[s * kRowsPerTile + row] = total;
-      }
+      const float total = shared_tile ? sum_partials<kOut>(a, rbs[k], clo[k], chi[k], s, row) : warp_total(k, s, row);
+      deliver<F, N, E>(a, epi, rbs[k], s, row, total);
     }
     if constexpr (E != Epi::Plain) {
       named_barrier(kBarConsumers, kConsumerThreads);
-      if constexpr (E == Epi::GateUp) gateup_epilogue<kOut>(a, tile_out, scale, wsum, rbs[k], tid, kConsumerThreads);
-      else down_epilogue<kOut>(a, tile_out, scale, wsum, rbs[k], tid, kConsumerThreads);
+      run_epilogue<kOut, E>(a, epi, rbs[k], tid, kConsumerThreads);
       epilogue_ran = true;
     }
+  }
+}
+
+// Adds the partials of the shared row tiles of a GEMV launch (one CTA per
+// row tile; tiles a single CTA computed were written by the GEMV) and runs
+// the fused epilogue on them.  Launched right after the GEMV with
+// programmatic dependent launch: it is resident early and waits for the GEMV
+// to complete.
+constexpr int kCombineThreads = 512;
+
+template <Fmt F, int N, Epi E>
+__global__ void __launch_bounds__(kCombineThreads) combine_tiles_kernel(const __grid_constant__ GemvArgs a) {
+  constexpr int kOut = Traits<F, N>::kOut;
+  __shared__ float epi[kEpiBytes / 4];
+  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
+  pdl_launch_dependents();
+  pdl_wait_primary();
+  const int32_t rb = static_cast<int32_t>(blockIdx.x);
+  const int32_t c_lo = cta_of_unit(static_cast<int64_t>(rb) * a.n_sb, a.units, a.grid);
+  const int32_t c_hi = cta_of_unit(static_cast<int64_t>(rb + 1) * a.n_sb - 1, a.units, a.grid);
+  if (c_hi == c_lo) return;  // written by the GEMV
+  if constexpr (E != Epi::Plain) input_scales<kOut>(a, warp, lane, epi + 4 * kRowsPerTile);
+  for (int t = tid; t < kOut * kRowsPerTile; t += kCombineThreads) {
+    const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
+    deliver<F, N, E>(a, epi, rb, s, row, sum_partials<kOut>(a, rb, c_lo, c_hi, s, row));
+  }
+  if constexpr (E != Epi::Plain) {
+    named_barrier(kBarConsumers, kCombineThreads);
+    run_epilogue<kOut, E>(a, epi, rb, tid, kCombineThreads);
   }
 }
 
@@ -953,11 +999,10 @@ inline size_t partial_bytes(int kout) {
   return static_cast<size_t>(kMaxGrid) * 2 * kout * kRowsPerTile * sizeof(float);
 }
 
-template <Fmt F>
-size_t fast_workspace_bytes(int64_t rows, int kout) {
-  const int64_t n_rb = (rows + kRowsPerTile - 1) / kRowsPerTile;
-  const size_t tickets = static_cast<size_t>(n_rb) * sizeof(unsigned int);
-  return (partial_bytes(kout) + tickets + 255) & ~static_cast<size_t>(255);
+// Workspace of the fast GEMV paths: the partials of shared tiles only (no
+// counters, so it needs no initialisation).
+inline size_t fast_workspace_bytes(int kout) {
+  return (partial_bytes(kout) + 255) & ~static_cast<size_t>(255);
 }
 
 // Encodes the 2-D tensor map of a row-major matrix of `rows` rows of
@@ -1019,6 +1064,7 @@ pti_status launch_gemv(const void *w, const void *w2, GemvArgs a, cudaStream_t s
   a.n_rb = static_cast<int32_t>(p.n_rb);
   a.grid = p.grid;
   a.stages = p.stages;
+  a.combine_in_kernel = 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
   cfg.blockDim = dim3(T::kWarps * 32 + 32);
@@ -1030,6 +1076,17 @@ pti_status launch_gemv(const void *w, const void *w2, GemvArgs a, cudaStream_t s
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   if (cudaLaunchKernelEx(&cfg, gemv_tma_kernel<F, N, E>, tmap, tmap2, a) != cudaSuccess) return launch_status();
+  // the shared tiles' partials, once the GEMV has completed (only if a tile
+  // spans several CTAs: never when every CTA owns whole tiles)
+  if (p.grid > 1) {
+    cudaLaunchConfig_t cc = {};
+    cc.gridDim = dim3(static_cast<unsigned>(p.n_rb));
+    cc.blockDim = dim3(kCombineThreads);
+    cc.stream = stream;
+    cc.attrs = attr;
+    cc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cc, combine_tiles_kernel<F, N, E>, a) != cudaSuccess) return launch_status();
+  }
   return launch_status();
 }
 
@@ -1043,7 +1100,6 @@ pti_status launch_fast(const void *w, int64_t rows, int64_t cols, const float *x
   a.y0 = y0;
   a.y1 = y1;
   a.part = static_cast<float *>(workspace);
-  a.tickets = reinterpret_cast<unsigned int *>(static_cast<uint8_t *>(workspace) + partial_bytes(Traits<F, N>::kOut));
   a.rows = rows;
   a.cols = cols;
   return launch_gemv<F, N, Epi::Plain>(w, nullptr, a, stream, pdl);

@@ -177,22 +177,25 @@ def test_decode_pass_64_layers(capsys):
               f"rms of the output {np.sqrt(np.mean(ref * ref)):.3g}")
 
 
-def test_decode_pass_is_deterministic_in_place_and_leaves_workspace_zero():
+@pytest.mark.parametrize("persistent", [False, True])
+def test_decode_pass_is_deterministic_in_place_and_needs_no_workspace_init(persistent):
     hidden, ffn, n = 768, 1280, 4
     layers = host_layers(2, hidden, ffn, seed=4)
     w = device_weights(layers)
     x = dev(pti_synth.activations(n, hidden, 4, 1000))
     need = pti.mlp_decode_pass_workspace_bytes(hidden, ffn, n)
-    ws = torch.zeros(need + 4096, dtype=torch.uint8, device="cuda")
-    a = pti.mlp_decode_pass(w, hidden, ffn, x, ws=ws)
-    b = pti.mlp_decode_pass(w, hidden, ffn, x, ws=ws)
+    ws = torch.full((need + 4096,), 255, dtype=torch.uint8, device="cuda")  # NaN patterns everywhere
+    a = pti.mlp_decode_pass(w, hidden, ffn, x, ws=ws, persistent=persistent)
+    b = pti.mlp_decode_pass(w, hidden, ffn, x, ws=ws, persistent=persistent)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
-    assert int(torch.count_nonzero(ws)) == 0
     xi = x.clone()
-    pti.mlp_decode_pass(w, hidden, ffn, xi, x_out=xi, ws=ws)
+    pti.mlp_decode_pass(w, hidden, ffn, xi, x_out=xi, ws=ws, persistent=persistent)
     torch.cuda.synchronize()
     assert torch.equal(xi, a)
+    xo, tol = layer_tolerance(*layers[1], hidden, ffn,
+                              run_pass(w, 1, hidden, ffn, x, persistent=persistent).astype(np.float32))
+    check_layer(a.cpu().numpy(), xo, tol, "layer 2 on a garbage-filled workspace")
     # the same workspace then serves a plain GEMV of another shape
     wq = dev(pti_synth.q8_matrix(1000, 2048, 4, 77))
     xq = dev(pti_synth.activations(3, 2048, 4, 78))

@@ -269,12 +269,12 @@ def test_twin_matches_q8_on_unpacked_models():
     assert np.all(np.abs(yb.cpu().numpy().astype(np.float64) - rb) <= 2 * TOL * bb)
 
 
-def test_workspace_reuse_across_calls():
-    """Every call leaves the workspace ready for the next one: three calls in a
-    row on one fresh zeroed workspace all match the oracle."""
+def test_workspace_needs_no_initialisation():
+    """The workspace is scratch: three calls in a row on one workspace filled
+    with 0xFF bytes (NaN patterns) all match the oracle."""
     rows, cols = 1000, 2048
     need = pti.q8_gemv_workspace_bytes(rows, cols, 4)
-    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    ws = torch.full((need,), 255, dtype=torch.uint8, device="cuda")
     w_np = pti_synth.q8_matrix(rows, cols, seed=2)
     w = dev(w_np)
     for k in range(3):
@@ -285,10 +285,9 @@ def test_workspace_reuse_across_calls():
 
 
 def test_one_workspace_serves_every_shape_and_stream_count():
-    """One zero-filled workspace shared, in turn, by Q8 calls of different shapes
-    and stream counts and by twin calls: every call matches the oracle (each call
-    must leave the whole workspace zero-filled for the next one)."""
-    ws = torch.zeros(pti.q8_gemv_workspace_bytes(5120, 17408, 4), dtype=torch.uint8, device="cuda")
+    """One workspace shared, in turn, by Q8 calls of different shapes and stream
+    counts and by twin calls: every call matches the oracle."""
+    ws = torch.full((pti.q8_gemv_workspace_bytes(5120, 17408, 4),), 255, dtype=torch.uint8, device="cuda")
     cases = [("q8", 1000, 2048, 4), ("q8", 520, 1024, 1), ("twin", 520, 1024, 2), ("q8", 1000, 2048, 2),
              ("twin", 1000, 2048, 2), ("q8", 520, 1024, 3), ("q8", 1000, 2048, 1)]
     for k, (kind, rows, cols, n) in enumerate(cases):
@@ -305,8 +304,6 @@ def test_one_workspace_serves_every_shape_and_stream_count():
             ra, rb, ba, bb = oracle.twin_gemv(w, rows, cols, xa, xb)
             assert_parity(ya.cpu().numpy(), ra, ba, f"case {k} A")
             assert_parity(yb.cpu().numpy(), rb, bb, f"case {k} B")
-    torch.cuda.synchronize()
-    assert int(ws.count_nonzero()) == 0
 
 
 def test_unaligned_activations_take_the_plain_path():

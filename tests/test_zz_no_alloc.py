@@ -26,8 +26,8 @@ def test_noalloc_entry_point_matches_the_workspace_entry_point_on_two_calls():
     pti.build()
     L = pti.lib()
     stream = torch.cuda.current_stream().cuda_stream
-    # two calls in a row with different shapes and stream counts: the second
-    # relies on the first leaving the shared scratch zero-filled
+    # two calls in a row with different shapes and stream counts share the
+    # built-in scratch
     for call, (rows, cols, n) in enumerate(((1000, 2048, 4), (520, 1024, 1))):
         w_np = pti_synth.q8_matrix(rows, cols, seed=300 + call)
         x_np = pti_synth.activations(n, cols, seed=310 + call)
@@ -44,14 +44,18 @@ def test_noalloc_entry_point_matches_the_workspace_entry_point_on_two_calls():
     assert pti.device_error() == 0
 
 
-def test_noalloc_rejects_shapes_beyond_its_scratch():
+def test_noalloc_scratch_covers_every_shape():
+    """The fast path's scratch depends only on the stream count, so the 2 MiB
+    array serves every valid shape; the entry point still validates its
+    arguments like the workspace entry point."""
     pti.build()
     L = pti.lib()
     limit = L.pti_q8_gemv_noalloc_max_scratch_bytes()
     assert limit == 2 << 20
-    fake = 0x7F0000000000  # never dereferenced: the size check fails first
-    rows = 25_165_824 + 128  # one 128-row tile more than 2 MiB serves at 4 streams
-    assert L.pti_q8_gemv_workspace_bytes(rows, 256, 4) > limit
-    rc = L.pti_q8_gemv_nstream_noalloc(fake, rows, 256, 4, fake + (1 << 36), fake + (2 << 36), None)
-    assert rc == 7  # PTI_ERR_WORKSPACE
-    assert L.pti_q8_gemv_workspace_bytes(25_165_824, 256, 4) <= limit
+    for rows, cols in ((1 << 31, 256), (1, 1 << 31), (17408, 5120)):
+        for n in (1, 2, 3, 4):
+            assert L.pti_q8_gemv_workspace_bytes(rows, cols, n) <= limit
+    fake = 0x7F0000000000  # never dereferenced: validation fails first
+    assert L.pti_q8_gemv_nstream_noalloc(None, 128, 512, 4, fake, fake + (1 << 36), None) == 1
+    assert L.pti_q8_gemv_nstream_noalloc(fake, 128, 48, 4, fake + (1 << 36), fake + (2 << 36), None) == 2
+    assert L.pti_q8_gemv_nstream_noalloc(fake, 128, 512, 5, fake + (1 << 36), fake + (2 << 36), None) == 3
