@@ -227,37 +227,45 @@ class Q8Pass:
 
 
 class TwinPass(Q8Pass):
-    def __init__(self, rows=17408, cols=5120, layers=8, seed=0):
+    """SSQ twin GEMV over L distinct twin matrices, `per_model` streams of each
+    model (per_model = 2: four tokens per weight load)."""
+
+    def __init__(self, rows=17408, cols=5120, layers=8, seed=0, per_model=1):
         import torch
         import pti_synth
         import stream_quantized_gemv_gb300 as pti
         self.pti, self.torch = pti, torch
-        self.rows, self.cols, self.n, self.layers = rows, cols, 2, layers
-        self.name = f"ssq_twin_gemv_{rows}x{cols}_x{layers}"
+        self.rows, self.cols, self.layers, self.per_model = rows, cols, layers, per_model
+        self.n = 2 * per_model
+        self.name = (f"ssq_twin_gemv_{rows}x{cols}_x{layers}" if per_model == 1
+                     else f"ssq_twin_gemv_n{per_model}_{rows}x{cols}_x{layers}")
         self.w = [pti_synth.twin_matrix_device(rows, cols, seed, 2000 + i) for i in range(layers)]
-        self.x = pti_synth.activations_device(2, cols, seed, 2)
-        self.y = torch.empty((2, rows), dtype=torch.float32, device="cuda")
-        need = pti.ssq_twin_gemv_workspace_bytes(rows, cols)
+        self.x = pti_synth.activations_device(self.n, cols, seed, 2)
+        self.y = torch.empty((self.n, rows), dtype=torch.float32, device="cuda")
+        need = pti.lib().pti_ssq_twin_gemv_nstream_workspace_bytes(rows, cols, per_model)
         self.ws = torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda")
         self.weight_bytes = rows * (cols // 32) * TWIN_BLOCK
-        self.launch_bytes = self.weight_bytes + 4 * 2 * (rows + cols)
+        self.launch_bytes = self.weight_bytes + 4 * self.n * (rows + cols)
         self.step_bytes = layers * self.launch_bytes
         self.launches_per_step = layers
-        self.tokens_per_step = 2
-        self.dominant = "gemv_tma_kernel<Twin>"
+        self.tokens_per_step = self.n
+        self.dominant = f"gemv_tma_kernel<Twin,{per_model}>"
         self.dtype = "f32"
 
     def step(self, x=None, y=None):
         x = self.x if x is None else x
         y = self.y if y is None else y
+        m = self.per_model
         for k, w in enumerate(self.w):
-            self.pti.ssq_twin_gemv(w, self.rows, self.cols, x[0], x[1], y_a=y[0], y_b=y[1], ws=self.ws,
-                                   flags=self.pti.FLAG_PDL if k > 0 else 0)
+            self.pti.ssq_twin_gemv_nstream(w, self.rows, self.cols, x[:m], x[m:], y_a=y[:m], y_b=y[m:], ws=self.ws,
+                                           flags=self.pti.FLAG_PDL if k > 0 else 0)
 
     def config(self):
         return {"workload": f"SSQ mode-16 twin GEMV: {self.layers} distinct {self.rows}x{self.cols} twin "
-                            "matrices (68-byte blocks), streams A and B",
+                            f"matrices (68-byte blocks), {self.per_model} stream(s) of model A and of model B, "
+                            "launches after the first with programmatic dependent launch",
                 "rows": self.rows, "cols": self.cols, "matrices_per_step": self.layers,
+                "streams_per_model": self.per_model,
                 "weight_bytes_per_step": self.layers * self.weight_bytes,
                 "l2": f"inputs larger than L2: {self.layers * self.weight_bytes / 1e9:.2f} GB per step"}
 
@@ -266,12 +274,14 @@ class TwinPass(Q8Pass):
         import pti_synth
         rows = 48
         w = pti_synth.twin_matrix(rows, self.cols, seed=0, tensor_id=1)
-        xa, xb = pti_synth.activations(2, self.cols, seed=0, tensor_id=2)
-        sample_bytes = rows * (self.cols // 32) * TWIN_BLOCK + 8 * (rows + self.cols)
+        x = pti_synth.activations(self.n, self.cols, seed=0, tensor_id=2)
+        m = self.per_model
+        sample_bytes = rows * (self.cols // 32) * TWIN_BLOCK + 4 * self.n * (rows + self.cols)
 
         def run():
-            oracle.twin_gemv(w, rows, self.cols, xa, xb)
-        return run, sample_bytes, f"oracle twin_gemv on {rows} of the {self.rows} rows"
+            for s in range(m):
+                oracle.twin_gemv(w, rows, self.cols, x[s], x[m + s])
+        return run, sample_bytes, f"oracle twin_gemv on {rows} of the {self.rows} rows, {m} stream(s) per model"
 
 
 class VerifyBatch(Q8Pass):
@@ -378,6 +388,7 @@ WORKLOADS = {
     "decode": lambda a: DecodePass(a.cols or 5120, a.rows or 17408, a.n, a.layers or 64),
     "q8": lambda a: Q8Pass(a.rows or 17408, a.cols or 5120, a.n, a.layers or 16),
     "twin": lambda a: TwinPass(a.rows or 17408, a.cols or 5120, a.layers or 8),
+    "twin2": lambda a: TwinPass(a.rows or 17408, a.cols or 5120, a.layers or 8, per_model=2),
     "verify": lambda a: VerifyBatch(),
 }
 
@@ -563,7 +574,7 @@ class _CpuOnly:
 
 def _cpu_only_workload(name, a):
     """The workload's config and CPU sample without allocating device memory."""
-    cls = {"decode": DecodePass, "q8": Q8Pass, "twin": TwinPass, "verify": VerifyBatch}[name]
+    cls = {"decode": DecodePass, "q8": Q8Pass, "twin": TwinPass, "twin2": TwinPass, "verify": VerifyBatch}[name]
     wl = cls.__new__(cls)
     if name == "decode":
         wl.hidden, wl.ffn, wl.n, wl.layers = a.cols or 5120, a.rows or 17408, a.n, a.layers or 64
@@ -571,8 +582,9 @@ def _cpu_only_workload(name, a):
     elif name == "q8":
         wl.rows, wl.cols, wl.n, wl.layers = a.rows or 17408, a.cols or 5120, a.n, a.layers or 16
         wl.weight_bytes = wl.rows * (wl.cols // 32) * Q8_BLOCK
-    elif name == "twin":
-        wl.rows, wl.cols, wl.n, wl.layers = a.rows or 17408, a.cols or 5120, 2, a.layers or 8
+    elif name in ("twin", "twin2"):
+        wl.per_model = 2 if name == "twin2" else 1
+        wl.rows, wl.cols, wl.n, wl.layers = a.rows or 17408, a.cols or 5120, 2 * wl.per_model, a.layers or 8
         wl.weight_bytes = wl.rows * (wl.cols // 32) * TWIN_BLOCK
     else:
         wl.steps, wl.n, wl.vocab, wl.p = 4096, 4, 151936, 0.6

@@ -173,6 +173,31 @@ pti_status pti_ssq_twin_gemv(const void *w_twin, int64_t rows, int64_t cols,
                              void *workspace, size_t workspace_bytes,
                              pti_stream_t stream);
 
+/*
+ * Twin GEMV with several streams per model: one pass over the packed twin
+ * matrix serves n_streams activation vectors of model A and n_streams of
+ * model B, y_A[s] = W_A x_A[s] and y_B[s] = W_B x_B[s].  With n_streams = 2,
+ * one weight load serves four tokens ([PTI-forum] §"未来发展方向": the PTI +
+ * MTP plan of four tokens per weight load; here the two extra tokens come
+ * from a second stream per twin, e.g. two speculative positions).
+ *
+ *   n_streams  1 or 2 per model (n_streams = 1 is pti_ssq_twin_gemv_ex).
+ *   x_a, x_b   [n_streams][cols] fp32 each, stream-major.
+ *   y_a, y_b   [n_streams][rows] fp32 out each; distinct, overlapping no input.
+ *   workspace  pti_ssq_twin_gemv_nstream_workspace_bytes(rows, cols, n_streams)
+ *              bytes of scratch (as for the other GEMVs).
+ *   flags      PTI_FLAG_PDL or 0.
+ * Other arguments, the fast-path condition and the error bound as for
+ * pti_ssq_twin_gemv.  A caller with an unequal number of streams per model
+ * passes a copy of one vector twice.
+ */
+size_t pti_ssq_twin_gemv_nstream_workspace_bytes(int64_t rows, int64_t cols, int n_streams);
+
+pti_status pti_ssq_twin_gemv_nstream(const void *w_twin, int64_t rows, int64_t cols, int n_streams,
+                                     const float *x_a, const float *x_b, float *y_a, float *y_b,
+                                     void *workspace, size_t workspace_bytes,
+                                     pti_stream_t stream, uint32_t flags);
+
 /* pti_ssq_twin_gemv with launch flags (PTI_FLAG_PDL, see above). */
 pti_status pti_ssq_twin_gemv_ex(const void *w_twin, int64_t rows, int64_t cols,
                                 const float *x_a, const float *x_b, float *y_a, float *y_b,

@@ -11,6 +11,7 @@ Functions (same names as the C ABI, without the ``pti_`` prefix):
 
 * ``q8_gemv_nstream(w, rows, cols, x)``      -> y [n][rows]
 * ``ssq_twin_gemv(w, rows, cols, x_a, x_b)``  -> (y_a, y_b)
+* ``ssq_twin_gemv_nstream(w, rows, cols, x_a, x_b)`` -> (y_a [n][rows], y_b [n][rows])
 * ``verify_greedy(logits, guess)``            -> (argmax, match, accept_len)
 * ``mlp_decode_pass(w_gate, w_up, w_down, hidden, ffn, x)`` -> x after the layers
 * ``device_error()``                          -> device error word (0 = none)
@@ -69,6 +70,10 @@ def lib() -> ctypes.CDLL:
             L.pti_q8_gemv_nstream_ex.argtypes = [P, I64, I64, I, P, P, P, SZ, P, ctypes.c_uint32]
             L.pti_ssq_twin_gemv_ex.restype = I
             L.pti_ssq_twin_gemv_ex.argtypes = [P, I64, I64, P, P, P, P, P, SZ, P, ctypes.c_uint32]
+            L.pti_ssq_twin_gemv_nstream.restype = I
+            L.pti_ssq_twin_gemv_nstream.argtypes = [P, I64, I64, I, P, P, P, P, P, SZ, P, ctypes.c_uint32]
+            L.pti_ssq_twin_gemv_nstream_workspace_bytes.restype = SZ
+            L.pti_ssq_twin_gemv_nstream_workspace_bytes.argtypes = [I64, I64, I]
             L.pti_ssq_twin_gemv_workspace_bytes.restype = SZ
             L.pti_ssq_twin_gemv_workspace_bytes.argtypes = [I64, I64]
             L.pti_ssq_twin_gemv.restype = I
@@ -169,6 +174,25 @@ def ssq_twin_gemv(w, rows: int, cols: int, x_a, x_b, y_a=None, y_b=None, ws=None
     _check(lib().pti_ssq_twin_gemv_ex(_ptr(w), rows, cols, _ptr(x_a), _ptr(x_b), _ptr(y_a), _ptr(y_b),
                                       _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                                       _stream(stream), flags), "pti_ssq_twin_gemv")
+    return y_a, y_b
+
+
+def ssq_twin_gemv_nstream(w, rows: int, cols: int, x_a, x_b, y_a=None, y_b=None, ws=None, stream=None,
+                          flags: int = 0):
+    """(y_A[s], y_B[s]) = (W_A x_A[s], W_B x_B[s]) for the n = x_a.shape[0]
+    (1 or 2) streams per model, from one pass over the packed twin matrix."""
+    import torch
+    n = x_a.shape[0]
+    if y_a is None:
+        y_a = torch.empty((n, rows), dtype=torch.float32, device=x_a.device)
+    if y_b is None:
+        y_b = torch.empty((n, rows), dtype=torch.float32, device=x_a.device)
+    need = lib().pti_ssq_twin_gemv_nstream_workspace_bytes(rows, cols, n)
+    if ws is None:
+        ws = workspace(need, x_a.device)
+    _check(lib().pti_ssq_twin_gemv_nstream(_ptr(w), rows, cols, n, _ptr(x_a), _ptr(x_b), _ptr(y_a), _ptr(y_b),
+                                           _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                                           _stream(stream), flags), "pti_ssq_twin_gemv_nstream")
     return y_a, y_b
 
 

@@ -130,6 +130,12 @@ extern "C" size_t pti_ssq_twin_gemv_workspace_bytes(int64_t rows, int64_t cols) 
   return fast_workspace_bytes(2);
 }
 
+extern "C" size_t pti_ssq_twin_gemv_nstream_workspace_bytes(int64_t rows, int64_t cols, int n_streams) {
+  if (check_gemv_shape(rows, cols) != PTI_OK || n_streams < 1 || n_streams > 2) return 0;
+  if (cols % 128 != 0) return 0;
+  return fast_workspace_bytes(2 * n_streams);
+}
+
 namespace {
 pti_status q8_gemv(const void *w_q8, int64_t rows, int64_t cols, int n_streams, const float *x, float *y,
                    void *workspace, size_t workspace_bytes, pti_stream_t stream, uint32_t flags) {
@@ -168,24 +174,28 @@ pti_status q8_gemv(const void *w_q8, int64_t rows, int64_t cols, int n_streams, 
   }
 }
 
-pti_status twin_gemv(const void *w_twin, int64_t rows, int64_t cols, const float *x_a, const float *x_b, float *y_a,
-                     float *y_b, void *workspace, size_t workspace_bytes, pti_stream_t stream, uint32_t flags) {
+// Twin GEMV with n activation streams per model (x_a, x_b [n][cols];
+// y_a, y_b [n][rows]).
+pti_status twin_gemv(const void *w_twin, int64_t rows, int64_t cols, int n, const float *x_a, const float *x_b,
+                     float *y_a, float *y_b, void *workspace, size_t workspace_bytes, pti_stream_t stream,
+                     uint32_t flags) {
   if ((flags & ~PTI_FLAG_PDL) != 0u) return PTI_ERR_VALUE;
   const bool pdl = (flags & PTI_FLAG_PDL) != 0u;
   if (w_twin == nullptr || x_a == nullptr || x_b == nullptr || y_a == nullptr || y_b == nullptr)
     return PTI_ERR_NULL;
   if (const pti_status s = check_gemv_shape(rows, cols); s != PTI_OK) return s;
+  if (n < 1 || n > 2) return PTI_ERR_NSTREAMS;
   if (!aligned(w_twin, 16) || !aligned(x_a, 4) || !aligned(x_b, 4) || !aligned(y_a, 4) || !aligned(y_b, 4))
     return PTI_ERR_ALIGN;
   const uint64_t w_bytes = static_cast<uint64_t>(rows) * (cols / 32) * 68;
-  const uint64_t x_bytes = static_cast<uint64_t>(cols) * 4;
-  const uint64_t y_bytes = static_cast<uint64_t>(rows) * 4;
+  const uint64_t x_bytes = static_cast<uint64_t>(n) * cols * 4;
+  const uint64_t y_bytes = static_cast<uint64_t>(n) * rows * 4;
   if (overlaps(y_a, y_bytes, y_b, y_bytes) || overlaps(y_a, y_bytes, w_twin, w_bytes) ||
       overlaps(y_b, y_bytes, w_twin, w_bytes) || overlaps(y_a, y_bytes, x_a, x_bytes) ||
       overlaps(y_a, y_bytes, x_b, x_bytes) || overlaps(y_b, y_bytes, x_a, x_bytes) ||
       overlaps(y_b, y_bytes, x_b, x_bytes))
     return PTI_ERR_ALIAS;
-  const size_t need = pti_ssq_twin_gemv_workspace_bytes(rows, cols);
+  const size_t need = (check_gemv_shape(rows, cols) == PTI_OK && cols % 128 == 0) ? fast_workspace_bytes(2 * n) : 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (need > 0) {
     if (workspace == nullptr || workspace_bytes < need) return PTI_ERR_WORKSPACE;
@@ -194,15 +204,21 @@ pti_status twin_gemv(const void *w_twin, int64_t rows, int64_t cols, const float
         overlaps(workspace, need, x_b, x_bytes) || overlaps(workspace, need, y_a, y_bytes) ||
         overlaps(workspace, need, y_b, y_bytes))
       return PTI_ERR_ALIAS;
-    if (aligned(x_a, 16) && aligned(x_b, 16))
+    if (aligned(x_a, 16) && aligned(x_b, 16) && (n == 1 || (cols * 4) % 16 == 0)) {
+      if (n == 1) return launch_fast<Fmt::Twin, 1>(w_twin, rows, cols, x_a, x_b, y_a, y_b, workspace, st, pdl);
       return launch_fast<Fmt::Twin, 2>(w_twin, rows, cols, x_a, x_b, y_a, y_b, workspace, st, pdl);
+    }
   }
   const int sms = current_device_sms();
   if (sms <= 0) return PTI_ERR_CUDA;
   const int64_t blocks = std::min<int64_t>((rows + 7) / 8, static_cast<int64_t>(sms) * 16);
-  twin_rowwise_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<const uint8_t *>(w_twin), rows, cols,
-                                                                     x_a, x_b, y_a, y_b);
-  return launch_status();
+  for (int s = 0; s < n; ++s) {
+    twin_rowwise_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        static_cast<const uint8_t *>(w_twin), rows, cols, x_a + static_cast<int64_t>(s) * cols,
+        x_b + static_cast<int64_t>(s) * cols, y_a + static_cast<int64_t>(s) * rows, y_b + static_cast<int64_t>(s) * rows);
+    if (const pti_status e = launch_status(); e != PTI_OK) return e;
+  }
+  return PTI_OK;
 }
 
 }  // namespace
@@ -222,13 +238,20 @@ extern "C" pti_status pti_q8_gemv_nstream_ex(const void *w_q8, int64_t rows, int
 extern "C" pti_status pti_ssq_twin_gemv(const void *w_twin, int64_t rows, int64_t cols, const float *x_a,
                                         const float *x_b, float *y_a, float *y_b, void *workspace,
                                         size_t workspace_bytes, pti_stream_t stream) {
-  return twin_gemv(w_twin, rows, cols, x_a, x_b, y_a, y_b, workspace, workspace_bytes, stream, 0u);
+  return twin_gemv(w_twin, rows, cols, 1, x_a, x_b, y_a, y_b, workspace, workspace_bytes, stream, 0u);
 }
 
 extern "C" pti_status pti_ssq_twin_gemv_ex(const void *w_twin, int64_t rows, int64_t cols, const float *x_a,
                                            const float *x_b, float *y_a, float *y_b, void *workspace,
                                            size_t workspace_bytes, pti_stream_t stream, uint32_t flags) {
-  return twin_gemv(w_twin, rows, cols, x_a, x_b, y_a, y_b, workspace, workspace_bytes, stream, flags);
+  return twin_gemv(w_twin, rows, cols, 1, x_a, x_b, y_a, y_b, workspace, workspace_bytes, stream, flags);
+}
+
+extern "C" pti_status pti_ssq_twin_gemv_nstream(const void *w_twin, int64_t rows, int64_t cols, int n_streams,
+                                                const float *x_a, const float *x_b, float *y_a, float *y_b,
+                                                void *workspace, size_t workspace_bytes, pti_stream_t stream,
+                                                uint32_t flags) {
+  return twin_gemv(w_twin, rows, cols, n_streams, x_a, x_b, y_a, y_b, workspace, workspace_bytes, stream, flags);
 }
 
 // ---------------------------------------------------------------------------

@@ -99,12 +99,13 @@ struct Traits<Fmt::Q8, N> {
   static constexpr int kXStreams = N;
   static constexpr int kBlockBytes = 34;
 };
+// Twin: N activation streams per model (model A's streams first, then B's).
 template <int N>
 struct Traits<Fmt::Twin, N> {
-  static constexpr int kOut = 2;
+  static constexpr int kOut = 2 * N;
   static constexpr int kWarps = kWarpCount;
   static constexpr int kColsPerSB = 128;
-  static constexpr int kXStreams = 2;
+  static constexpr int kXStreams = 2 * N;
   static constexpr int kBlockBytes = 68;
 };
 
@@ -119,10 +120,10 @@ struct Stage {
 };
 
 struct GemvArgs {
-  const float *x0;  // Q8: x [N][cols]; twin: x_a
-  const float *x1;  // twin: x_b
-  float *y0;        // Q8: y [N][rows]; twin: y_a
-  float *y1;        // twin: y_b
+  const float *x0;  // Q8: x [N][cols]; twin: x_a [N][cols]
+  const float *x1;  // twin: x_b [N][cols]
+  float *y0;        // Q8: y [N][rows]; twin: y_a [N][rows]
+  float *y1;        // twin: y_b [N][rows]
   float *part;      // workspace: [grid][2 slots][kOut][128] partial sums
   unsigned int *tickets;  // in-kernel combining only: [n_rb] arrival counters, zero at start
   int64_t rows, cols, units;  // GateUp: rows = gate rows = up rows = outputs per stream
@@ -253,7 +254,7 @@ __device__ __forceinline__ void q8_body(const uint8_t *tile, const ChunkParams &
 // chunk holds column pair cpbase + j (before the scale word) or cpbase + j - 1.
 template <int N, int J>
 __device__ __forceinline__ void twin_body(const uint8_t *tile, const ChunkParams &cp, const uint8_t *xsb,
-                                          uint32_t lane, uint32_t half, uint64_t (&acc)[kTaskSlots][2]) {
+                                          uint32_t lane, uint32_t half, uint64_t (&acc)[kTaskSlots][2 * N]) {
   constexpr int J0 = (J == 0) ? 1 : 0;
   uint4 w[kTaskSlots];
   ScalePair sa_lo[kTaskSlots], sb_lo[kTaskSlots], sa_hi[kTaskSlots], sb_hi[kTaskSlots];
@@ -273,34 +274,43 @@ __device__ __forceinline__ void twin_body(const uint8_t *tile, const ChunkParams
     }
   }
   const uint8_t *xc = xsb + cp.cpbase * 8;
-  uint64_t pa[kTaskSlots], pb[kTaskSlots];
+  uint64_t pa[kTaskSlots][N], pb[kTaskSlots][N];
   static_for<0, 4>([&](auto jc) {
     constexpr int j = decltype(jc)::value;
     if constexpr (j != J) {
       constexpr int off = (J >= 0 && j > J) ? j - 1 : j;
-      const uint64_t xa = *reinterpret_cast<const uint64_t *>(xc + off * 8);
-      const uint64_t xb = *reinterpret_cast<const uint64_t *>(xc + Stage<Fmt::Twin, N>::kXStreamBytes + off * 8);
+      uint64_t xa[N], xb[N];
+#pragma unroll
+      for (int s = 0; s < N; ++s) {
+        xa[s] = *reinterpret_cast<const uint64_t *>(xc + s * Stage<Fmt::Twin, N>::kXStreamBytes + off * 8);
+        xb[s] = *reinterpret_cast<const uint64_t *>(xc + (N + s) * Stage<Fmt::Twin, N>::kXStreamBytes + off * 8);
+      }
       constexpr bool lo = (J < 0 || j < J);
 #pragma unroll
       for (int r = 0; r < kTaskSlots; ++r) {
         const uint32_t wxj = word_at<j>(w[r]) ^ 0x80808080u;
         const uint64_t wa = dequant2(wxj, 1, wxj, 3, lo ? sa_lo[r] : sa_hi[r]);  // model A: high bytes
         const uint64_t wb = dequant2(wxj, 0, wxj, 2, lo ? sb_lo[r] : sb_hi[r]);  // model B: low bytes
-        if constexpr (j == J0) {
-          pa[r] = fmul2(wa, xa);
-          pb[r] = fmul2(wb, xb);
-        } else {
-          pa[r] = ffma2(wa, xa, pa[r]);
-          pb[r] = ffma2(wb, xb, pb[r]);
+#pragma unroll
+        for (int s = 0; s < N; ++s) {
+          if constexpr (j == J0) {
+            pa[r][s] = fmul2(wa, xa[s]);
+            pb[r][s] = fmul2(wb, xb[s]);
+          } else {
+            pa[r][s] = ffma2(wa, xa[s], pa[r][s]);
+            pb[r][s] = ffma2(wb, xb[s], pb[r][s]);
+          }
         }
       }
     }
   });
 #pragma unroll
-  for (int r = 0; r < kTaskSlots; ++r) {
-    acc[r][0] = fadd2(acc[r][0], pa[r]);
-    acc[r][1] = fadd2(acc[r][1], pb[r]);
-  }
+  for (int r = 0; r < kTaskSlots; ++r)
+#pragma unroll
+    for (int s = 0; s < N; ++s) {
+      acc[r][s] = fadd2(acc[r][s], pa[r][s]);
+      acc[r][N + s] = fadd2(acc[r][N + s], pb[r][s]);
+    }
 }
 
 // One Q8 block b of the super-block (columns 32b .. 32b+31) for the lane's
@@ -527,7 +537,8 @@ __device__ __forceinline__ void deliver(const GemvArgs &a, float *tile_out, int3
     const int64_t row_g = static_cast<int64_t>(rb) * kRowsPerTile + row;
     if (row_g < a.rows) {
       if constexpr (F == Fmt::Q8) a.y0[s * a.rows + row_g] = total;
-      else (s == 0 ? a.y0 : a.y1)[row_g] = total;
+      else if (s < N) a.y0[s * a.rows + row_g] = total;  // model A's streams, then B's
+      else a.y1[(s - N) * a.rows + row_g] = total;
     }
   } else {
     tile_out[s * kRowsPerTile + row] = total;
@@ -780,8 +791,15 @@ struct Producer {
                   a->x0 + static_cast<int64_t>(st) * a->cols + static_cast<int64_t>(sb) * T::kColsPerSB,
                   S::kXStreamBytes, bar);
     } else {
-      bulk_load(xdst, a->x0 + static_cast<int64_t>(sb) * T::kColsPerSB, S::kXStreamBytes, bar);
-      bulk_load(xdst + S::kXStreamBytes, a->x1 + static_cast<int64_t>(sb) * T::kColsPerSB, S::kXStreamBytes, bar);
+#pragma unroll
+      for (int st = 0; st < N; ++st) {
+        bulk_load(xdst + st * S::kXStreamBytes,
+                  a->x0 + static_cast<int64_t>(st) * a->cols + static_cast<int64_t>(sb) * T::kColsPerSB,
+                  S::kXStreamBytes, bar);
+        bulk_load(xdst + (N + st) * S::kXStreamBytes,
+                  a->x1 + static_cast<int64_t>(st) * a->cols + static_cast<int64_t>(sb) * T::kColsPerSB,
+                  S::kXStreamBytes, bar);
+      }
     }
   }
   // Weights do not depend on the previous kernel in the stream: fetch the

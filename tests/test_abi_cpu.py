@@ -173,3 +173,15 @@ def test_decode_pass_ex_rejects_unknown_flags(L):
     assert L.pti_mlp_decode_pass_ex(*args, 1) == 8 and L.pti_mlp_decode_pass_ex(*args, 4) == 8
     assert L.pti_mlp_decode_pass_ex(gate, up, down, 0, *args[4:], 2) == 2
     assert L.pti_mlp_decode_pass_ex(gate, up, down, 4097, *args[4:], 0) == 2
+
+
+def test_twin_nstream_validation(L):
+    args = (FAKE, 128, 512)
+    xa, xb, ya, yb = FAKE + (1 << 30), FAKE + (1 << 30) + 4096, FAKE + (2 << 30), FAKE + (2 << 30) + 8192
+    assert L.pti_ssq_twin_gemv_nstream(*args, 0, xa, xb, ya, yb, FAKE + (3 << 30), 1 << 24, None, 0) == 3
+    assert L.pti_ssq_twin_gemv_nstream(*args, 3, xa, xb, ya, yb, FAKE + (3 << 30), 1 << 24, None, 0) == 3
+    assert L.pti_ssq_twin_gemv_nstream(*args, 2, xa, xb, ya, yb, FAKE + (3 << 30), 1 << 24, None, 8) == 8
+    assert L.pti_ssq_twin_gemv_nstream(*args, 2, xa, xb, ya, ya + 512, FAKE + (3 << 30), 1 << 24, None, 0) == 5
+    assert L.pti_ssq_twin_gemv_nstream(*args, 2, xa, xb, ya, yb, None, 0, None, 0) == 7
+    assert L.pti_ssq_twin_gemv_nstream_workspace_bytes(128, 512, 2) > L.pti_ssq_twin_gemv_nstream_workspace_bytes(128, 512, 1)
+    assert L.pti_ssq_twin_gemv_nstream_workspace_bytes(128, 512, 3) == 0

@@ -255,6 +255,52 @@ def test_identical_twins_give_identical_outputs(rows, cols):
     assert_parity(ya.cpu().numpy()[idx], ya_ref, ba, "identical twins")
 
 
+@pytest.mark.parametrize("rows,cols", [(1, 128), (130, 384), (256, 512), (1000, 2048), (7, 224)])
+@pytest.mark.parametrize("n", [1, 2])
+def test_twin_nstream_matches_oracle(rows, cols, n):
+    """n streams per model: every stream of A and of B matches the oracle's twin
+    GEMV on that stream pair (fast path for cols % 128 == 0, plain otherwise)."""
+    w = pti_synth.twin_matrix(rows, cols, seed=rows + n)
+    xa = pti_synth.activations(n, cols, seed=rows + n, tensor_id=1)
+    xb = pti_synth.activations(n, cols, seed=rows + n, tensor_id=2)
+    ya, yb = pti.ssq_twin_gemv_nstream(dev(w), rows, cols, dev(xa), dev(xb))
+    ya, yb = ya.cpu().numpy(), yb.cpu().numpy()
+    for s in range(n):
+        ra, rb, ba, bb = oracle.twin_gemv(w, rows, cols, xa[s], xb[s])
+        assert_parity(ya[s], ra, ba, f"A stream {s}")
+        assert_parity(yb[s], rb, bb, f"B stream {s}")
+
+
+@pytest.mark.parametrize("rows,cols", [(17408, 5120), (5120, 17408)])
+def test_twin_two_streams_per_model_full_size(full_twin, rows, cols):
+    """Four tokens per weight load: two streams of each twin at full size,
+    every row tile sampled; stream 0 equals the one-stream call within the bar."""
+    w_np = full_twin[(rows, cols)]
+    w = dev(w_np)
+    xa = pti_synth.activations(2, cols, seed=0, tensor_id=400)
+    xb = pti_synth.activations(2, cols, seed=0, tensor_id=401)
+    ya, yb = pti.ssq_twin_gemv_nstream(w, rows, cols, dev(xa), dev(xb))
+    ya, yb = ya.cpu().numpy(), yb.cpu().numpy()
+    idx = tile_sample_rows(rows, np.random.default_rng(rows + 2))
+    for s in range(2):
+        ra, rb, ba, bb = oracle.twin_gemv(w_np, rows, cols, xa[s], xb[s], rows_idx=idx)
+        assert_parity(ya[s, idx], ra, ba, f"A stream {s}")
+        assert_parity(yb[s, idx], rb, bb, f"B stream {s}")
+    y1a, y1b = pti.ssq_twin_gemv(w, rows, cols, dev(xa[0]), dev(xb[0]))
+    _, _, ba, bb = oracle.twin_gemv(w_np, rows, cols, xa[0], xb[0], rows_idx=idx)
+    assert np.all(np.abs(ya[0, idx].astype(np.float64) - y1a.cpu().numpy()[idx]) <= 2 * TOL * ba)
+    assert np.all(np.abs(yb[0, idx].astype(np.float64) - y1b.cpu().numpy()[idx]) <= 2 * TOL * bb)
+
+
+def test_twin_two_streams_identical_twins_and_streams():
+    """A == B and x_A[s] == x_B[s]: y_A[s] == y_B[s] bit for bit for both streams."""
+    rows, cols = 1000, 2048
+    w = pti_synth.twin_matrix(rows, cols, seed=3, tensor_id=9, identical=True)
+    x = pti_synth.activations(2, cols, seed=3, tensor_id=10)
+    ya, yb = pti.ssq_twin_gemv_nstream(dev(w), rows, cols, dev(x), dev(x))
+    assert torch.equal(ya, yb)
+
+
 def test_twin_matches_q8_on_unpacked_models():
     """Cross-kernel: twin(T, x_a, x_b) agrees with the Q8 GEMV of each unpacked model."""
     rows, cols = 520, 1024
