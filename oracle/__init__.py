@@ -76,6 +76,8 @@ def _load():
             lib.pti_or_twin_gemv_rows.argtypes = [P, I64, I64, P, P, P, I64, P, P, P, P]
             lib.pti_or_verify_greedy.restype = I
             lib.pti_or_verify_greedy.argtypes = [P, P, I64, I, I64, P, P, P]
+            lib.pti_or_verify_sample.restype = I
+            lib.pti_or_verify_sample.argtypes = [P, P, P, I64, I, I64, ctypes.c_double, P, P, P, P, P]
             lib.pti_or_mlp_layer.restype = I
             lib.pti_or_mlp_layer.argtypes = [P, P, P, I64, I64, I, ctypes.c_double, P, P, P]
             _lib = lib
@@ -189,6 +191,31 @@ def verify_greedy(logits: np.ndarray, guess: np.ndarray):
     _check(_load().pti_or_verify_greedy(_ptr(logits), _ptr(guess), steps, n, vocab,
                                         _ptr(argmax), match_ptr, _ptr(accept)), "verify_greedy")
     return argmax, match, accept
+
+
+def verify_sample(logits: np.ndarray, guess: np.ndarray, uniform: np.ndarray, temperature: float):
+    """Sampling-mode verify.  ``logits`` [steps][n][vocab] float32, ``guess``
+    [steps][n] int32, ``uniform`` [steps][n] float32 in [0, 1).
+
+    Returns ``(token, match, accept, collision, margin)``: the inverse-CDF draws
+    [steps][n] int32, match [steps][n-1] uint8, accept [steps] int32, the
+    collision probabilities and the draws' margins [steps][n] float64.
+    """
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    guess = np.ascontiguousarray(guess, dtype=np.int32)
+    uniform = np.ascontiguousarray(uniform, dtype=np.float32)
+    steps, n, vocab = logits.shape
+    if guess.shape != (steps, n) or uniform.shape != (steps, n):
+        raise ValueError("verify_sample: guess or uniform has the wrong shape")
+    token = np.empty((steps, n), dtype=np.int32)
+    match = np.empty((steps, max(n - 1, 0)), dtype=np.uint8)
+    accept = np.empty(steps, dtype=np.int32)
+    collision = np.empty((steps, n), dtype=np.float64)
+    margin = np.empty((steps, n), dtype=np.float64)
+    _check(_load().pti_or_verify_sample(_ptr(logits), _ptr(guess), _ptr(uniform), steps, n, vocab,
+                                        float(temperature), _ptr(token), _ptr(match), _ptr(accept),
+                                        _ptr(collision), _ptr(margin)), "verify_sample")
+    return token, match, accept, collision, margin
 
 
 def mlp_layer(wg, wu, wd, hidden: int, ffn: int, x: np.ndarray, eps: float = 1e-6):

@@ -268,6 +268,91 @@ int pti_or_verify_greedy(const float *logits, const int32_t *guess, int64_t step
 }
 
 /* ---------------------------------------------------------------------------
+ * Sampling-mode verify ([PTI-readme] §"接受机制如何工作", the temperature > 0
+ * case): at temperature T each stream's output distribution is
+ * p(v) = exp(l_v / T) / sum_u exp(l_u / T); the stream draws its token from p,
+ * and the guess fed to stream s+1 is accepted when it equals stream s's draw.
+ * Two independent draws from the same p agree with probability sum_v p(v)^2,
+ * the collision probability the pages give as the acceptance rate.
+ *
+ * The draw is the inverse-CDF one for the supplied uniform number u in
+ * [0, 1): the smallest v with p(0) + ... + p(v) > u.  (The random numbers are
+ * inputs, so the draw is a plain function of them.)  The exponentials are
+ * taken after subtracting the row maximum, which changes no ratio.
+ * margin[t][s] = min(u - CDF(v - 1), CDF(v) - u) for the drawn v: how far u
+ * lies from the edges of the drawn token's interval.
+ * ------------------------------------------------------------------------- */
+int pti_or_verify_sample(const float *logits, const int32_t *guess, const float *uniform,
+                         int64_t steps, int n, int64_t vocab, double temperature,
+                         int32_t *token, uint8_t *match, int32_t *accept, double *collision,
+                         double *margin)
+{
+    int64_t t, v;
+    int s;
+    double *e;
+    if (logits == NULL || guess == NULL || uniform == NULL || token == NULL || accept == NULL)
+        return -1;
+    if (steps < 0 || n < 1 || vocab < 1 || (n > 1 && match == NULL))
+        return -1;
+    if (!(temperature > 0.0) || !isfinite(temperature))
+        return -1;
+    e = (double *)malloc((size_t)vocab * sizeof(double));
+    if (e == NULL)
+        return -1;
+
+    for (t = 0; t < steps; ++t) {
+        int run = 1;
+        int32_t accepted = 0;
+        for (s = 0; s < n; ++s) {
+            const float *row = logits + (t * n + s) * vocab;
+            const double u = (double)uniform[t * n + s];
+            double top = (double)row[0], total = 0.0, squares = 0.0, cum = 0.0, below = 0.0;
+            int64_t drawn = -1;
+            for (v = 1; v < vocab; ++v)
+                if ((double)row[v] > top)
+                    top = (double)row[v];
+            for (v = 0; v < vocab; ++v) {
+                e[v] = exp(((double)row[v] - top) / temperature);
+                total += e[v];
+                squares += e[v] * e[v];
+            }
+            for (v = 0; v < vocab; ++v) {
+                below = cum;
+                cum += e[v] / total;
+                if (cum > u) {
+                    drawn = v;
+                    break;
+                }
+            }
+            if (drawn < 0) {  /* u at or above the last rounded CDF value: the last token with mass */
+                for (v = vocab - 1; v > 0 && e[v] == 0.0; --v) {
+                }
+                drawn = v;
+                below = cum - e[v] / total;
+            }
+            token[t * n + s] = (int32_t)drawn;
+            if (collision != NULL)
+                collision[t * n + s] = squares / (total * total);
+            if (margin != NULL) {
+                const double hi = below + e[drawn] / total;
+                margin[t * n + s] = (u - below < hi - u) ? u - below : hi - u;
+            }
+        }
+        for (s = 0; s + 1 < n; ++s) {
+            uint8_t m = (uint8_t)(guess[t * n + s + 1] == token[t * n + s]);
+            match[t * (n - 1) + s] = m;
+            if (run && m)
+                ++accepted;
+            else
+                run = 0;
+        }
+        accept[t] = accepted;
+    }
+    free(e);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
  * One gated-MLP layer of the multi-stream decode weight pass.  The pages'
  * step loads every weight once for N tokens ([PTI-readme] §"工作原理");
  * the gated MLP (W_up, W_gate, W_down) is the one of [CS336-L10] §"2.4 MLP 层

@@ -95,6 +95,21 @@ int pti_or_twin_gemv_rows(const uint8_t *w, int64_t rows, int64_t cols,
 int pti_or_verify_greedy(const float *logits, const int32_t *guess, int64_t steps, int n,
                          int64_t vocab, int32_t *argmax, uint8_t *match, int32_t *accept);
 
+/* Sampling-mode verify at temperature > 0 ([PTI-readme] §"接受机制如何工作").
+ *   logits [steps][n][vocab]; guess [steps][n] (guess[t][0] is not read);
+ *   uniform [steps][n] in [0, 1): the random number of each stream's draw.
+ *   token [steps][n]      inverse-CDF draw from p = softmax(logits / temperature):
+ *                         the smallest v with p(0) + ... + p(v) > u
+ *   match [steps][n-1], accept [steps]  as for the greedy verify, on the draws
+ *   collision [steps][n]  sum_v p(v)^2 (may be NULL)
+ *   margin [steps][n]     distance of u from the edges of the drawn token's
+ *                         CDF interval (may be NULL)
+ * Returns 0, or -1 on a bad argument (temperature must be finite and > 0). */
+int pti_or_verify_sample(const float *logits, const int32_t *guess, const float *uniform,
+                         int64_t steps, int n, int64_t vocab, double temperature,
+                         int32_t *token, uint8_t *match, int32_t *accept, double *collision,
+                         double *margin);
+
 /* One layer of the multi-stream decode weight pass (gated MLP, RMS rescale):
  *   g = Wg x, u = Wu x            (Wg, Wu: [ffn][hidden] Q8)
  *   h = SiLU(g) * u, SiLU(v) = v / (1 + exp(-v))

@@ -447,4 +447,126 @@ def test_mlp_layer_zero_weights_give_zero():
     d = 32
     z = _diag_q8(d, 0)
     x_out, h = oracle.mlp_layer(z, z, z, d, d, pti_synth.activations(1, d, 1))
-    assert not x_out.any() and not h.any()
+    assert not x_out.any() and not h.any()# ---------------------------------------------------------------------------
+# Sampling-mode verify ([PTI-readme] §接受机制如何工作, temperature > 0)
+# ---------------------------------------------------------------------------
+def _one_row(logits, u, temperature):
+    lg = np.asarray(logits, np.float32)[None, None, :]
+    tok, _, _, col, margin = oracle.verify_sample(lg, np.zeros((1, 1), np.int32),
+                                                  np.array([[u]], np.float32), temperature)
+    return int(tok[0, 0]), float(col[0, 0]), float(margin[0, 0])
+
+
+def test_sample_uniform_logits_is_floor_u_v():
+    """Equal logits: p = 1/V, the draw is floor(u V) and the collision 1/V."""
+    for vocab in (1, 2, 7, 1000, 151936):
+        for u in (0.0, 0.1234, 0.5 + 0.25 / vocab, 0.9999):
+            tok, col, _ = _one_row(np.full(vocab, 3.5), u, 0.7)
+            assert tok == min(vocab - 1, math.floor(np.float32(u) * vocab)), (vocab, u, tok)
+            assert abs(col - 1.0 / vocab) <= 1e-12
+
+
+def test_sample_two_tokens_closed_form():
+    """Two tokens: p0 = 1 / (1 + exp((b - a) / T)); the draw is 0 iff u < p0 and
+    the collision p0^2 + (1 - p0)^2."""
+    for a, b, temp in ((0.0, 1.0, 1.0), (2.0, -1.0, 0.5), (1.0, 1.0, 3.0), (-4.0, 4.0, 2.0)):
+        p0 = 1.0 / (1.0 + math.exp((b - a) / temp))
+        for u in (0.05, p0 - 1e-4, p0 + 1e-4, 0.95):
+            if not 0.0 <= u < 1.0:
+                continue
+            tok, col, _ = _one_row([a, b], u, temp)
+            assert tok == (0 if np.float32(u) < p0 else 1)
+            assert abs(col - (p0 * p0 + (1 - p0) ** 2)) <= 1e-12
+
+
+def test_sample_low_temperature_is_argmax():
+    rng = np.random.default_rng(4)
+    for _ in range(20):
+        row = rng.normal(0, 1, 500).astype(np.float32)
+        for u in (1e-3, 0.5, 0.999):  # u = 0 would pick the first token with any (tiny) mass
+            tok, col, _ = _one_row(row, u, 1e-4)
+            assert tok == int(np.argmax(row)) and col > 1 - 1e-9
+
+
+def test_sample_stratified_grid_reproduces_p():
+    """Inverse-CDF draws at u_k = (k + 1/2) / K hit token v exactly K p(v) times,
+    up to one at each interval edge."""
+    logits = np.array([0.3, -1.2, 2.0, 0.0, 1.1, -0.4, 0.9], np.float32)
+    temp, K = 0.8, 4000
+    e = np.exp((logits.astype(np.float64) - logits.max()) / temp)
+    p = e / e.sum()
+    u = ((np.arange(K) + 0.5) / K).astype(np.float32)
+    lg = np.broadcast_to(logits, (K, 1, logits.size)).copy()
+    tok, _, _, col, margin = oracle.verify_sample(lg, np.zeros((K, 1), np.int32), u[:, None], temp)
+    counts = np.bincount(tok[:, 0], minlength=logits.size)
+    assert np.all(np.abs(counts - K * p) <= 1.0 + 1e-9), (counts, K * p)
+    assert np.all(margin >= 0.0)
+    assert np.allclose(col, np.sum(p * p), rtol=0, atol=1e-14)
+
+
+def test_sample_temperature_scaling_invariance():
+    """Doubling the logits and the temperature changes nothing (exact in fp32)."""
+    rng = np.random.default_rng(5)
+    lg = rng.normal(0, 2, (6, 3, 300)).astype(np.float32)
+    u = rng.random((6, 3)).astype(np.float32)
+    g = np.zeros((6, 3), np.int32)
+    a = oracle.verify_sample(lg, g, u, 0.6)
+    b = oracle.verify_sample(lg * np.float32(2.0), g, u, 1.2)
+    assert np.array_equal(a[0], b[0])
+    assert np.allclose(a[3], b[3], rtol=1e-12, atol=0)
+
+
+def test_sample_acceptance_is_the_collision_probability():
+    """The pages' rule: a guess drawn from the same distribution as the stream's
+    own draw is accepted with probability sum_x p(x)^2.  Monte Carlo over rows of
+    various entropies: the accept rate of stream 0's draw against an independent
+    draw from an identical row lies within 4 standard errors of the mean
+    collision probability."""
+    rng = np.random.default_rng(6)
+    steps, vocab = 6000, 40
+    lg = np.empty((steps, 2, vocab), np.float32)
+    base = rng.normal(0, 1.5, (steps, vocab)).astype(np.float32)
+    lg[:, 0], lg[:, 1] = base, base
+    u = rng.random((steps, 2)).astype(np.float32)
+    # the guess for stream 1 is an independent draw from the same row
+    g_tok, _, _, _, _ = oracle.verify_sample(lg[:, 1:2].copy(), np.zeros((steps, 1), np.int32), u[:, 1:2].copy(), 0.9)
+    guess = np.zeros((steps, 2), np.int32)
+    guess[:, 1] = g_tok[:, 0]
+    tok, match, accept, col, _ = oracle.verify_sample(lg, guess, u, 0.9)
+    rate = match[:, 0].mean()
+    q = col[:, 0]
+    se = math.sqrt(float(np.mean(q * (1 - q))) / steps)
+    assert abs(rate - q.mean()) <= 4 * se + 1e-12, (rate, q.mean(), se)
+    assert np.array_equal(accept, match[:, 0].astype(np.int32))
+
+
+def test_sample_accept_chain_and_margins():
+    """Guesses planted equal to the draws are all accepted; a mismatch at stream
+    s stops the run there; every draw lies inside its CDF interval."""
+    rng = np.random.default_rng(7)
+    steps, n, vocab = 50, 4, 64
+    lg = rng.normal(0, 2, (steps, n, vocab)).astype(np.float32)
+    u = rng.random((steps, n)).astype(np.float32)
+    tok, _, _, _, margin = oracle.verify_sample(lg, np.zeros((steps, n), np.int32), u, 1.3)
+    guess = np.zeros((steps, n), np.int32)
+    guess[:, 1:] = tok[:, :-1]
+    _, match, accept, _, _ = oracle.verify_sample(lg, guess, u, 1.3)
+    assert np.all(match == 1) and np.all(accept == n - 1)
+    guess[:, 2] = (tok[:, 1] + 1) % vocab
+    _, match, accept, _, _ = oracle.verify_sample(lg, guess, u, 1.3)
+    assert np.all(accept == 1) and np.all(match[:, 1] == 0) and np.all(match[:, 2] == 1)
+    e = np.exp((lg.astype(np.float64) - lg.max(axis=2, keepdims=True)) / 1.3)
+    cdf = np.cumsum(e / e.sum(axis=2, keepdims=True), axis=2)
+    hi = np.take_along_axis(cdf, tok[..., None], 2)[..., 0]
+    lo = hi - np.take_along_axis(e / e.sum(axis=2, keepdims=True), tok[..., None], 2)[..., 0]
+    assert np.all(lo <= u + 1e-12) and np.all(u < hi + 1e-12) and np.all(margin >= 0)
+
+
+def test_sample_rejects_bad_temperature():
+    lg = np.zeros((1, 1, 4), np.float32)
+    for temp in (0.0, -1.0, float("inf"), float("nan")):
+        with pytest.raises(ValueError):
+            oracle.verify_sample(lg, np.zeros((1, 1), np.int32), np.zeros((1, 1), np.float32), temp)
+
+
+
