@@ -5,7 +5,7 @@ and up (17408 x 5120) and down (5120 x 17408) GEMVs with the SiLU and RMS
 glue, N = 4 fp32 activation streams chained layer to layer; one step = one
 pass over all 18.2 GB of distinct weights (each byte read once per step).
 Other lines: ``--workload q8`` (the N-stream Q8 GEMV over distinct
-17408 x 5120 matrices), ``twin``, ``verify``, ``all``.
+17408 x 5120 matrices), ``twin``, ``twin2``, ``verify``, ``verify_sample``, ``all``.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -325,6 +325,64 @@ class VerifyBatch(Q8Pass):
         return run, b, f"oracle verify_greedy on {steps} of the {self.steps} steps"
 
 
+class VerifySampleBatch(Q8Pass):
+    """Sampling-mode verify of a batch: inverse-CDF draws from softmax(l / T)
+    per stream, acceptance against guesses and sum p^2 (one step = one batch)."""
+
+    def __init__(self, steps=4096, n=4, vocab=151936, temperature=1.0, seed=0):
+        import torch
+        import pti_synth
+        import stream_quantized_gemv_gb300 as pti
+        self.pti, self.torch = pti, torch
+        self.steps, self.n, self.vocab, self.temperature = steps, n, vocab, temperature
+        self.name = f"verify_sample_{steps}x{n}x{vocab}"
+        self.logits, self.uniform = pti_synth.sample_batch_device(steps, n, vocab, seed)
+        _, u2 = pti_synth.sample_batch_device(steps, n, 1, seed + 1)
+        # guesses: independent draws from the same rows (the draft the pages'
+        # acceptance rule assumes), so about sum p^2 of them are accepted
+        zeros = torch.zeros((steps, n), dtype=torch.int32, device="cuda")
+        t2, _, _, _ = pti.verify_sample(self.logits, zeros, u2, temperature, collision=False)
+        self.guess = torch.zeros_like(zeros)
+        self.guess[:, 1:] = t2[:, :-1]
+        del t2, u2
+        self.out = (torch.empty((steps, n), dtype=torch.int32, device="cuda"),
+                    torch.empty((steps, n - 1), dtype=torch.uint8, device="cuda"),
+                    torch.empty(steps, dtype=torch.int32, device="cuda"),
+                    torch.empty((steps, n), dtype=torch.float32, device="cuda"))
+        self.launch_bytes = steps * n * vocab * 4 + steps * n * 4 * 2 + steps * n * 4 * 2 + steps * (n - 1) + steps * 4
+        self.step_bytes = self.launch_bytes
+        self.launches_per_step = 1
+        self.tokens_per_step = steps * n
+        self.dominant = "verify_sample_kernel"
+        self.dtype = "f32"
+        self.x = self.logits
+        self.y = self.out[2]
+
+    def step(self, x=None, y=None):
+        t, m, a, c = self.out
+        self.pti.verify_sample(self.logits, self.guess, self.uniform, self.temperature, token=t, match=m,
+                               accept=a, collision=c)
+
+    def config(self):
+        return {"workload": f"sampling verify batch {self.steps} steps x {self.n} streams x vocab {self.vocab}, "
+                            f"N(0,3) logits, T={self.temperature}, uniform draws, guesses drawn independently "
+                            "from the same rows",
+                "l2": f"inputs larger than L2: {self.launch_bytes / 1e9:.2f} GB of logits per step"}
+
+    def cpu_sample(self):
+        import numpy as np
+        import oracle
+        import pti_synth
+        steps = 16
+        lg, u = pti_synth.sample_batch(steps, self.n, self.vocab, seed=0)
+        gs = np.zeros((steps, self.n), np.int32)
+        b = steps * self.n * self.vocab * 4
+
+        def run():
+            oracle.verify_sample(lg, gs, u, self.temperature)
+        return run, b, f"oracle verify_sample on {steps} of the {self.steps} steps"
+
+
 class DecodePass(Q8Pass):
     """The chained decode weight pass: L layers of gate/up/down Q8 GEMVs with
     the fused SiLU and RMS glue, N streams (one step = one pass)."""
@@ -390,6 +448,7 @@ WORKLOADS = {
     "twin": lambda a: TwinPass(a.rows or 17408, a.cols or 5120, a.layers or 8),
     "twin2": lambda a: TwinPass(a.rows or 17408, a.cols or 5120, a.layers or 8, per_model=2),
     "verify": lambda a: VerifyBatch(),
+    "verify_sample": lambda a: VerifySampleBatch(),
 }
 
 
@@ -433,32 +492,42 @@ def time_gpu(wl, steps, warmup, world, local):
 
 def time_e2e(wl, steps, warmup):
     """Same pass through the public API with inputs in pinned host memory:
-    per step H2D of the activations, the pass, D2H of the result."""
+    per step H2D of the step's inputs, the pass, D2H of the result.  For the
+    verify batches the logits are the model's output, already on the device;
+    the host supplies the guesses (and, for sampling, the uniform numbers)."""
     import torch
-    if isinstance(wl, VerifyBatch):
-        hx = torch.empty_like(wl.guess, device="cpu").pin_memory()
-        hx.copy_(wl.guess.cpu())
-        dx = wl.guess
-        hy = torch.empty_like(wl.out[2], device="cpu").pin_memory()
-        dy = wl.out[2]
+
+    def pinned(d):
+        h = torch.empty_like(d, device="cpu").pin_memory()
+        h.copy_(d.cpu())
+        return h
+
+    if isinstance(wl, (VerifyBatch, VerifySampleBatch)):
+        ins = [(pinned(wl.guess), wl.guess)]
+        if isinstance(wl, VerifySampleBatch):
+            ins.append((pinned(wl.uniform), wl.uniform))
+        hy, dy = pinned(wl.out[2]), wl.out[2]
     else:
         hx, hy, dx, dy = wl.e2e_buffers()
+        ins = [(hx, dx)]
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
-        dx.copy_(hx, non_blocking=True)
+        for h, d in ins:
+            d.copy_(h, non_blocking=True)
         wl.step()
         hy.copy_(dy, non_blocking=True)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(steps):
-        dx.copy_(hx, non_blocking=True)
+        for h, d in ins:
+            d.copy_(h, non_blocking=True)
         wl.step()
         hy.copy_(dy, non_blocking=True)
     ev1.record(stream)
     torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1) / steps
-    return ms, hx.numel() * hx.element_size(), hy.numel() * hy.element_size()
+    return ms, sum(h.numel() * h.element_size() for h, _ in ins), hy.numel() * hy.element_size()
 
 
 def time_cpu(wl, budget_s=12.0):
@@ -574,7 +643,8 @@ class _CpuOnly:
 
 def _cpu_only_workload(name, a):
     """The workload's config and CPU sample without allocating device memory."""
-    cls = {"decode": DecodePass, "q8": Q8Pass, "twin": TwinPass, "twin2": TwinPass, "verify": VerifyBatch}[name]
+    cls = {"decode": DecodePass, "q8": Q8Pass, "twin": TwinPass, "twin2": TwinPass, "verify": VerifyBatch,
+           "verify_sample": VerifySampleBatch}[name]
     wl = cls.__new__(cls)
     if name == "decode":
         wl.hidden, wl.ffn, wl.n, wl.layers = a.cols or 5120, a.rows or 17408, a.n, a.layers or 64
@@ -586,6 +656,9 @@ def _cpu_only_workload(name, a):
         wl.per_model = 2 if name == "twin2" else 1
         wl.rows, wl.cols, wl.n, wl.layers = a.rows or 17408, a.cols or 5120, 2 * wl.per_model, a.layers or 8
         wl.weight_bytes = wl.rows * (wl.cols // 32) * TWIN_BLOCK
+    elif name == "verify_sample":
+        wl.steps, wl.n, wl.vocab, wl.temperature = 4096, 4, 151936, 1.0
+        wl.launch_bytes = wl.steps * wl.n * wl.vocab * 4
     else:
         wl.steps, wl.n, wl.vocab, wl.p = 4096, 4, 151936, 0.6
         wl.launch_bytes = wl.steps * wl.n * wl.vocab * 4

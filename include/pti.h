@@ -8,6 +8,8 @@
  *                         y_s = W x_s for 1..4 activation vectors x_s.
  *   pti_ssq_twin_gemv     SSQ "mode 16" twin GEMV: one pass over a packed twin
  *                         matrix computes y_A = W_A x_A and y_B = W_B x_B.
+ *   pti_verify_sample     sampling-mode verify: per-stream inverse-CDF draw from
+ *                         softmax(logits / T), acceptance and sum p^2.
  *   pti_verify_greedy     greedy verify: per-stream argmax, guess == actual and
  *                         the accepted-prefix length of every step.
  *   pti_mlp_decode_pass   a chained decode pass: n_layers gated-MLP layers
@@ -229,6 +231,43 @@ pti_status pti_verify_greedy(const float *logits, const int32_t *guess,
                              int64_t steps, int n_streams, int64_t vocab,
                              int32_t *argmax_out, uint8_t *match_out, int32_t *accept_len_out,
                              pti_stream_t stream);
+
+/*
+ * Sampling-mode verify.
+ *   [PTI-readme] §"接受机制如何工作", the temperature > 0 case: stream s's
+ *   output token is a draw from p_s = softmax(logits[t][s] / T); the guess fed
+ *   to stream s+1 is accepted when it equals stream s's draw, and acceptance
+ *   stops at the first mismatch.  A guess drawn independently from the same
+ *   distribution matches with probability sum_v p(v)^2 (the collision
+ *   probability), returned per stream.
+ *
+ *   logits      [steps][n_streams][vocab] fp32, 4-byte aligned (16-byte
+ *               aligned rows take the vector path).  -inf marks a token with
+ *               no mass; each row needs at least one finite logit, and NaN or
+ *               +inf give unspecified (but in-range) tokens.
+ *   guess       [steps][n_streams] int32; guess[t][0] is not read.
+ *   uniform     [steps][n_streams] fp32 in [0, 1): the random number of each
+ *               draw (supplied by the caller, so the draw is a plain function
+ *               of the inputs).  Other values give unspecified in-range tokens.
+ *   temperature T > 0, finite, with log2(e) / T finite in fp32 (else
+ *               PTI_ERR_VALUE).
+ *   token_out   [steps][n_streams] int32 out: the inverse-CDF draw, the
+ *               smallest v with p(0) + ... + p(v) > u, computed in fp32; when
+ *               u lies within fp32 rounding of an interval edge either
+ *               neighbouring token may be returned (always one with p > 0).
+ *               Results are deterministic.
+ *   match_out   [steps][n_streams-1] uint8 out, 1 when guess[t][s+1] ==
+ *               token[t][s]; may be NULL when n_streams == 1.
+ *   accept_len_out [steps] int32 out, the number of leading 1s of match.
+ *   collision_out  [steps][n_streams] fp32 out, sum_v p(v)^2, or NULL.
+ * steps == 0 enqueues nothing and returns PTI_OK once the scalars are valid.
+ * One CTA handles one step; each row is read once from HBM plus about a
+ * sixteenth of it again from L2.
+ */
+pti_status pti_verify_sample(const float *logits, const int32_t *guess, const float *uniform,
+                             int64_t steps, int n_streams, int64_t vocab, float temperature,
+                             int32_t *token_out, uint8_t *match_out, int32_t *accept_len_out,
+                             float *collision_out, pti_stream_t stream);
 
 /*
  * Chained decode pass over n_layers gated-MLP layers.

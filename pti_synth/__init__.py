@@ -25,7 +25,8 @@ Distributions (the workloads of the pages' Qwen3.6-27B measurements: hidden
 * block scales: ``u`` uniform on [0.5, 2), stored as binary16(u / 127) with
   round-to-nearest-even (numpy's float64 -> float16 conversion);
 * activations: N(0, 1) by Box-Muller in float64, rounded to float32;
-* logits: N(0, sigma) with one planted maximum per row.
+* logits: N(0, sigma) with one planted maximum per row (greedy verify), or
+  plain N(0, sigma) with uniform numbers on [0, 1) for the draws (sampling).
 """
 from __future__ import annotations
 
@@ -112,6 +113,13 @@ def index_uniform(seed: int, tensor_id: int, count: int, n: int) -> np.ndarray:
     return ((r >> np.uint64(32)) * np.uint64(n) >> np.uint64(32)).astype(np.int64)
 
 
+def uniform_f32(seed: int, tensor_id: int, count: int) -> np.ndarray:
+    """float32 uniform on [0, 1): the top 24 bits of each draw times 2^-24
+    (exact in float32, so 1.0 never occurs)."""
+    r = draws(seed, tensor_id, 0, count)
+    return ((r >> np.uint64(40)).astype(np.float64) * (1.0 / 16777216.0)).astype(np.float32)
+
+
 # --------------------------------------------------------------------------
 # Byte layouts
 # --------------------------------------------------------------------------
@@ -192,6 +200,25 @@ def verify_batch(steps: int, n: int, vocab: int, p: float, seed: int, tensor_id:
     return logits, guess, planted.astype(np.int32)
 
 
+def sample_batch(steps: int, n: int, vocab: int, seed: int, tensor_id: int = 0, sigma: float = 3.0,
+                 masked: float = 0.0):
+    """Sampling-verify inputs: logits [steps][n][vocab] float32 N(0, sigma^2)
+    and the draws' uniform numbers [steps][n] float32 on [0, 1).  With
+    ``masked`` > 0 about that fraction of the tokens is set to -inf (token 0
+    never is, so every row keeps a finite logit).  Guesses are left to the
+    caller: they are draws, which need the method's arithmetic.
+
+    Returns ``(logits, uniform)``.
+    """
+    logits = normal_f32(seed, 4 * tensor_id, steps * n * vocab, sigma).reshape(steps, n, vocab)
+    uniform = uniform_f32(seed, 4 * tensor_id + 1, steps * n).reshape(steps, n)
+    if masked > 0.0:
+        drop = _unit_from(draws(seed, 4 * tensor_id + 2, 0, steps * n * vocab)).reshape(steps, n, vocab) < masked
+        drop[:, :, 0] = False
+        logits[drop] = -np.inf
+    return logits, uniform
+
+
 # --------------------------------------------------------------------------
 # Device generators (torch Philox on the GPU) for multi-GB workloads
 # --------------------------------------------------------------------------
@@ -255,6 +282,18 @@ def activations_device(n: int, cols: int, seed: int, tensor_id: int, device="cud
     import torch
     g = _gen(device, seed, tensor_id)
     return torch.randn((n, cols), generator=g, device=device, dtype=torch.float32)
+
+
+def sample_batch_device(steps: int, n: int, vocab: int, seed: int, tensor_id: int = 0, sigma: float = 3.0,
+                        device="cuda"):
+    """``sample_batch`` drawn on the device (no masking): N(0, sigma^2) logits
+    and uniform numbers on [0, 1)."""
+    import torch
+    g = _gen(device, seed, tensor_id)
+    logits = torch.randn((steps, n, vocab), generator=g, device=device, dtype=torch.float32)
+    logits.mul_(sigma)
+    uniform = torch.rand((steps, n), generator=g, device=device, dtype=torch.float32)
+    return logits, uniform
 
 
 def verify_batch_device(steps: int, n: int, vocab: int, p: float, seed: int, tensor_id: int = 0,

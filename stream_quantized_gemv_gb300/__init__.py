@@ -3,7 +3,7 @@
 The compute lives in hand-written sm_103a CUDA kernels behind the C ABI of
 ``include/pti.h``.  This module only marshals arguments: it turns torch device
 tensors into pointers, passes torch's current CUDA stream, allocates the
-(zero-filled, reusable) workspace the fast paths need, and raises ``PTIError``
+(reusable scratch) workspace the fast paths need, and raises ``PTIError``
 on a non-OK status.  There is no fallback: if ``libpti.so`` has not been built
 the import of the native library fails loudly.
 
@@ -13,6 +13,7 @@ Functions (same names as the C ABI, without the ``pti_`` prefix):
 * ``ssq_twin_gemv(w, rows, cols, x_a, x_b)``  -> (y_a, y_b)
 * ``ssq_twin_gemv_nstream(w, rows, cols, x_a, x_b)`` -> (y_a [n][rows], y_b [n][rows])
 * ``verify_greedy(logits, guess)``            -> (argmax, match, accept_len)
+* ``verify_sample(logits, guess, uniform, temperature)`` -> (token, match, accept_len, collision)
 * ``mlp_decode_pass(w_gate, w_up, w_down, hidden, ffn, x)`` -> x after the layers
 * ``device_error()``                          -> device error word (0 = none)
 * ``lib()``                                   -> the ctypes handle of the C ABI
@@ -80,6 +81,8 @@ def lib() -> ctypes.CDLL:
             L.pti_ssq_twin_gemv.argtypes = [P, I64, I64, P, P, P, P, P, SZ, P]
             L.pti_verify_greedy.restype = I
             L.pti_verify_greedy.argtypes = [P, P, I64, I, I64, P, P, P, P]
+            L.pti_verify_sample.restype = I
+            L.pti_verify_sample.argtypes = [P, P, P, I64, I, I64, ctypes.c_float, P, P, P, P, P]
             L.pti_q8_gemv_noalloc_max_scratch_bytes.restype = SZ
             L.pti_q8_gemv_noalloc_max_scratch_bytes.argtypes = []
             L.pti_q8_gemv_nstream_noalloc.restype = I
@@ -211,6 +214,34 @@ def verify_greedy(logits, guess, argmax=None, match=None, accept=None, stream=No
     _check(lib().pti_verify_greedy(_ptr(logits), _ptr(guess), steps, n, vocab, _ptr(argmax), match_ptr,
                                    _ptr(accept), _stream(stream)), "pti_verify_greedy")
     return argmax, match, accept
+
+
+def verify_sample(logits, guess, uniform, temperature: float, token=None, match=None, accept=None,
+                  collision=None, stream=None):
+    """Sampling-mode verify of ``logits`` [steps][n][vocab] f32: inverse-CDF
+    draws from softmax(logits / temperature) with the supplied ``uniform``
+    [steps][n] f32 in [0, 1), matched against ``guess`` [steps][n] i32.
+
+    Returns ``(token [steps][n] i32, match [steps][n-1] u8, accept [steps] i32,
+    collision [steps][n] f32)``; pass ``collision=False`` to skip the collision
+    output."""
+    import torch
+    steps, n, vocab = logits.shape
+    dev = logits.device
+    if token is None:
+        token = torch.empty((steps, n), dtype=torch.int32, device=dev)
+    if match is None:
+        match = torch.empty((steps, max(n - 1, 0)), dtype=torch.uint8, device=dev)
+    if accept is None:
+        accept = torch.empty(steps, dtype=torch.int32, device=dev)
+    if collision is None:
+        collision = torch.empty((steps, n), dtype=torch.float32, device=dev)
+    col_ptr = _ptr(collision) if collision is not False else 0
+    match_ptr = _ptr(match) if n > 1 else 0
+    _check(lib().pti_verify_sample(_ptr(logits), _ptr(guess), _ptr(uniform), steps, n, vocab,
+                                   float(temperature), _ptr(token), match_ptr, _ptr(accept), col_ptr,
+                                   _stream(stream)), "pti_verify_sample")
+    return token, match, accept, (collision if collision is not False else None)
 
 
 def q8_gemv_nstream_noalloc(w, rows: int, cols: int, x, y=None, stream=None):

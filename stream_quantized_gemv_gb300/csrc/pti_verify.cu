@@ -1,4 +1,5 @@
-// pti_verify.cu -- greedy verify of self-speculative decoding on sm_103a.
+// pti_verify.cu -- greedy and sampling-mode verify of self-speculative
+// decoding on sm_103a.
 //
 // [PTI-readme] "打包双子推理（PTI）" §"接受机制如何工作": at each step stream 0
 // runs on the confirmed token and stream s on the guess for position n+s.  Under
@@ -16,6 +17,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <cmath>
 #include <cstdint>
 
 #include "pti.h"
@@ -115,6 +117,224 @@ __global__ void __launch_bounds__(kVerifyThreads)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Sampling-mode verify ([PTI-readme] §"接受机制如何工作", temperature > 0): each
+// stream draws its token from p = softmax(logits / T) by inverse CDF with the
+// supplied uniform u (the smallest v with p(0) + ... + p(v) > u); the guess
+// fed to stream s+1 is accepted when it equals stream s's draw; the collision
+// probability sum p^2 (the pages' acceptance rate) is returned per stream.
+//
+// One CTA per step.  Per row, warp w owns the contiguous segment
+// [w L, (w+1) L) of the vocabulary (L a multiple of 4, so segments start on
+// 16-byte boundaries).  Pass 1 streams the row once from HBM, four 16-byte
+// loads in flight per lane, keeping per lane an online maximum m with the sums
+// of 2^((x-m)c) and of its square (c = log2(e) / T, rescaled when m grows).
+// The warps' results give the row maximum M, the normaliser Z, sum e^2 / Z^2
+// and the segment masses.  The draw lies in the first segment whose running
+// mass exceeds u Z; pass 2 reads only that segment again (from L2) with the
+// whole block, each thread summing one contiguous run of it, then a
+// block-wide inclusive prefix sum over the runs.  The first thread whose
+// prefix exceeds the threshold walks its run again to the token.  (Float
+// rounding can make two warps claim when the threshold sits on a run edge;
+// the smaller token wins, so the result is deterministic.)
+// Logits may hold -inf (masked tokens, mass 0); each row needs one finite
+// logit.
+// ---------------------------------------------------------------------------
+constexpr int kSampleThreads = 512;
+constexpr int kSampleWarps = kSampleThreads / 32;
+constexpr int kSampleDepth = 4;  // 16-byte loads in flight per lane in pass 1
+
+struct OnlineSums {
+  float m, s, q;  // running maximum, sum of 2^((x-m)c), sum of its square
+};
+
+__device__ __forceinline__ void online_add4(OnlineSums &a, const float4 &v, float c) {
+  const float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+  if (!(mx > -INFINITY)) return;  // four masked tokens (or padding): no mass
+  if (mx > a.m) {
+    const float r = exp2f((a.m - mx) * c);  // a.m = -inf gives r = 0
+    a.s *= r;
+    a.q *= r * r;
+    a.m = mx;
+  }
+  const float e0 = exp2f((v.x - a.m) * c), e1 = exp2f((v.y - a.m) * c);
+  const float e2 = exp2f((v.z - a.m) * c), e3 = exp2f((v.w - a.m) * c);
+  a.s += (e0 + e1) + (e2 + e3);
+  a.q += (e0 * e0 + e1 * e1) + (e2 * e2 + e3 * e3);
+}
+
+__device__ __forceinline__ OnlineSums online_merge(OnlineSums a, OnlineSums b, float c) {
+  if (b.m > a.m) {
+    const OnlineSums t = a;
+    a = b;
+    b = t;
+  }
+  if (!(b.m > -INFINITY)) return a;
+  const float r = exp2f((b.m - a.m) * c);
+  a.s += b.s * r;
+  a.q += b.q * (r * r);
+  return a;
+}
+
+// Four logits from i on; positions at or past `end` read as -inf.  kVec: the
+// row base is 16-byte aligned and i is a multiple of 4.
+template <bool kVec>
+__device__ __forceinline__ float4 load4(const float *row, int64_t i, int64_t end) {
+  if (kVec && i + 3 < end) return __ldcg(reinterpret_cast<const float4 *>(row + i));
+  float4 v;
+  v.x = (i + 0 < end) ? __ldcg(row + i + 0) : -INFINITY;
+  v.y = (i + 1 < end) ? __ldcg(row + i + 1) : -INFINITY;
+  v.z = (i + 2 < end) ? __ldcg(row + i + 2) : -INFINITY;
+  v.w = (i + 3 < end) ? __ldcg(row + i + 3) : -INFINITY;
+  return v;
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kSampleThreads)
+    verify_sample_kernel(const float *__restrict__ logits, const int32_t *__restrict__ guess,
+                         const float *__restrict__ uniform, int64_t steps, int n, int64_t vocab, float c,
+                         int32_t *__restrict__ token_out, uint8_t *__restrict__ match_out,
+                         int32_t *__restrict__ accept_out, float *__restrict__ collision_out) {
+  __shared__ OnlineSums s_warp[kSampleWarps];
+  __shared__ float s_scan[kSampleWarps];
+  __shared__ int s_last[kSampleWarps];
+  __shared__ int s_tok[4];
+  __shared__ int s_seg;
+  __shared__ float s_theta, s_max;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t seg = ((vocab + 4 * kSampleWarps - 1) / (4 * kSampleWarps)) * 4;
+  const int64_t run_len = ((seg + 4 * kSampleThreads - 1) / (4 * kSampleThreads)) * 4;
+  for (int64_t t = blockIdx.x; t < steps; t += gridDim.x) {
+    for (int s = 0; s < n; ++s) {
+      const float *row = logits + (t * n + s) * vocab;
+      // ---- pass 1: this warp's segment, online maximum and sums
+      const int64_t lo = warp * seg, hi = min(lo + seg, vocab);
+      OnlineSums a{-INFINITY, 0.0f, 0.0f};
+      int64_t i = lo + 4 * lane;
+      for (; i + 32 * 4 * (kSampleDepth - 1) < hi; i += 32 * 4 * kSampleDepth) {
+        float4 v[kSampleDepth];
+#pragma unroll
+        for (int d = 0; d < kSampleDepth; ++d) v[d] = load4<kVec>(row, i + 128 * d, hi);
+#pragma unroll
+        for (int d = 0; d < kSampleDepth; ++d) online_add4(a, v[d], c);
+      }
+      for (; i < hi; i += 128) online_add4(a, load4<kVec>(row, i, hi), c);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        OnlineSums b;
+        b.m = __shfl_xor_sync(0xFFFFFFFFu, a.m, o);
+        b.s = __shfl_xor_sync(0xFFFFFFFFu, a.s, o);
+        b.q = __shfl_xor_sync(0xFFFFFFFFu, a.q, o);
+        a = online_merge(a, b, c);
+      }
+      if (lane == 0) s_warp[warp] = a;
+      __syncthreads();
+      // ---- row maximum, normaliser, collision; the segment holding the draw
+      if (tid == 0) {
+        float m = -INFINITY;
+        for (int w = 0; w < kSampleWarps; ++w) m = fmaxf(m, s_warp[w].m);
+        float z = 0.0f, q = 0.0f, cum[kSampleWarps];
+        int last_w = 0;
+        for (int w = 0; w < kSampleWarps; ++w) {
+          const float r = (s_warp[w].m > -INFINITY) ? exp2f((s_warp[w].m - m) * c) : 0.0f;
+          const float mass = s_warp[w].s * r;
+          if (mass > 0.0f) last_w = w;
+          z += mass;
+          q += s_warp[w].q * (r * r);
+          cum[w] = z;
+        }
+        if (collision_out != nullptr) collision_out[t * n + s] = q / (z * z);
+        const float theta = uniform[t * n + s] * z;
+        int w = 0;
+        while (w < kSampleWarps && !(cum[w] > theta)) ++w;
+        if (w == kSampleWarps) w = last_w;  // u Z at the end of the row within rounding
+        s_seg = w;
+        s_theta = theta - (w > 0 ? cum[w - 1] : 0.0f);  // >= 0: mass left to pass in the segment
+        s_max = m;
+        s_tok[s] = INT_MAX;
+      }
+      __syncthreads();
+      // ---- pass 2: the draw's segment again, thread k taking the k-th run of
+      // cl tokens; a block-wide prefix sum finds the run holding the draw, and
+      // that thread walks its run once more
+      const int64_t slo = s_seg * seg, shi = min(slo + seg, vocab);
+      const int64_t jlo = slo + tid * run_len, jhi = min(jlo + run_len, shi);
+      const float m = s_max, theta = s_theta;
+      float own = 0.0f;
+      int last = -1;  // last token of the run with mass (the rounding fallback)
+#pragma unroll 4
+      for (int64_t j = jlo; j < jhi; j += 4) {
+        const float4 v = load4<kVec>(row, j, jhi);
+        const float e0 = exp2f((v.x - m) * c), e1 = exp2f((v.y - m) * c);
+        const float e2 = exp2f((v.z - m) * c), e3 = exp2f((v.w - m) * c);
+        own += (e0 + e1) + (e2 + e3);
+        if (e3 > 0.0f) last = static_cast<int>(j + 3);
+        else if (e2 > 0.0f) last = static_cast<int>(j + 2);
+        else if (e1 > 0.0f) last = static_cast<int>(j + 1);
+        else if (e0 > 0.0f) last = static_cast<int>(j);
+      }
+      float incl = own;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      float prev = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+      if (lane == 0) prev = 0.0f;
+      if (lane == 31) s_scan[warp] = incl;
+      int lw = last;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lw = max(lw, __shfl_xor_sync(0xFFFFFFFFu, lw, o));
+      if (lane == 0) s_last[warp] = lw;
+      __syncthreads();
+      float before = 0.0f, total = 0.0f;
+      for (int w = 0; w < kSampleWarps; ++w) {
+        if (w == warp) before = total;
+        total += s_scan[w];
+      }
+      const bool over = before + incl > theta;
+      const unsigned ballot = __ballot_sync(0xFFFFFFFFu, over);
+      if (over && !(before > theta) && lane == __ffs(ballot) - 1) {
+        // the first thread of its warp whose prefix passes theta, in a warp whose
+        // predecessors' total does not: its run holds the draw
+        float cum = before + prev;
+        int k = -1;
+        for (int64_t j = jlo; j < jhi && k < 0; j += 4) {
+          const float4 v = load4<kVec>(row, j, jhi);
+          const float e[4] = {exp2f((v.x - m) * c), exp2f((v.y - m) * c), exp2f((v.z - m) * c),
+                              exp2f((v.w - m) * c)};
+          for (int d = 0; d < 4 && k < 0; ++d) {
+            cum += e[d];
+            if (cum > theta && e[d] > 0.0f) k = static_cast<int>(j + d);
+          }
+        }
+        const int cand = k >= 0 ? k : last;
+        if (cand >= 0) atomicMin(&s_tok[s], cand);
+      }
+      __syncthreads();
+      if (tid == 0 && s_tok[s] == INT_MAX) {  // u Z at the segment's end within rounding
+        int best = -1;
+        for (int w = 0; w < kSampleWarps; ++w) best = max(best, s_last[w]);
+        s_tok[s] = best >= 0 ? best : static_cast<int>(slo);
+      }
+      __syncthreads();
+      if (tid == 0) token_out[t * n + s] = s_tok[s];
+    }
+    if (tid == 0) {
+      int32_t accepted = 0;
+      bool run = true;
+      for (int s = 0; s + 1 < n; ++s) {
+        const bool mtc = guess[t * n + s + 1] == s_tok[s];
+        match_out[t * (n - 1) + s] = mtc ? 1 : 0;
+        if (run && mtc) ++accepted;
+        else run = false;
+      }
+      accept_out[t] = accepted;
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
 }  // namespace pti
 
@@ -155,5 +375,48 @@ extern "C" pti_status pti_verify_greedy(const float *logits, const int32_t *gues
   else
     verify_greedy_kernel<false><<<grid, kVerifyThreads, 0, st>>>(logits, guess, steps, n_streams, vocab,
                                                                   argmax_out, match_out, accept_len_out);
+  return launch_status();
+}
+
+extern "C" pti_status pti_verify_sample(const float *logits, const int32_t *guess, const float *uniform,
+                                        int64_t steps, int n_streams, int64_t vocab, float temperature,
+                                        int32_t *token_out, uint8_t *match_out, int32_t *accept_len_out,
+                                        float *collision_out, pti_stream_t stream) {
+  if (n_streams < 1 || n_streams > 4) return PTI_ERR_NSTREAMS;
+  if (steps < 0 || vocab < 1 || vocab > INT_MAX) return PTI_ERR_SHAPE;
+  if (steps > (int64_t{1} << 40) / (static_cast<int64_t>(n_streams) * vocab)) return PTI_ERR_SHAPE;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return PTI_ERR_VALUE;
+  const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));  // log2(e) / T
+  if (!std::isfinite(c)) return PTI_ERR_VALUE;
+  if (steps == 0) return PTI_OK;
+  if (logits == nullptr || guess == nullptr || uniform == nullptr || token_out == nullptr ||
+      accept_len_out == nullptr || (n_streams > 1 && match_out == nullptr))
+    return PTI_ERR_NULL;
+  if (!aligned(logits, 4) || !aligned(guess, 4) || !aligned(uniform, 4) || !aligned(token_out, 4) ||
+      !aligned(accept_len_out, 4) || !aligned(collision_out, 4))
+    return PTI_ERR_ALIGN;
+  const uint64_t l_bytes = static_cast<uint64_t>(steps) * n_streams * vocab * 4;
+  const uint64_t g_bytes = static_cast<uint64_t>(steps) * n_streams * 4;
+  const void *ins[3] = {logits, guess, uniform};
+  const uint64_t in_bytes[3] = {l_bytes, g_bytes, g_bytes};
+  void *outs[4] = {token_out, match_out, accept_len_out, collision_out};
+  const uint64_t out_bytes[4] = {g_bytes, n_streams > 1 ? static_cast<uint64_t>(steps) * (n_streams - 1) : 0,
+                                 static_cast<uint64_t>(steps) * 4, collision_out ? g_bytes : 0};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 3; ++j)
+      if (overlaps(outs[i], out_bytes[i], ins[j], in_bytes[j])) return PTI_ERR_ALIAS;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return PTI_ERR_ALIAS;
+  }
+  const int sms = current_device_sms();
+  if (sms <= 0) return PTI_ERR_CUDA;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(steps, static_cast<int64_t>(sms) * 4));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (aligned(logits, 16) && vocab % 4 == 0)
+    verify_sample_kernel<true><<<grid, kSampleThreads, 0, st>>>(logits, guess, uniform, steps, n_streams, vocab, c,
+                                                                token_out, match_out, accept_len_out, collision_out);
+  else
+    verify_sample_kernel<false><<<grid, kSampleThreads, 0, st>>>(logits, guess, uniform, steps, n_streams, vocab, c,
+                                                                 token_out, match_out, accept_len_out, collision_out);
   return launch_status();
 }

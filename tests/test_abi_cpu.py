@@ -29,7 +29,7 @@ def _declared_functions():
 
 def test_header_declares_the_documented_entry_points():
     names = _declared_functions()
-    for required in ("pti_q8_gemv_nstream", "pti_ssq_twin_gemv", "pti_verify_greedy",
+    for required in ("pti_q8_gemv_nstream", "pti_ssq_twin_gemv", "pti_verify_greedy", "pti_verify_sample",
                      "pti_status_string", "pti_device_error"):
         assert required in names
 
@@ -104,6 +104,28 @@ def test_verify_validation(L):
     assert _verify(L, logits=FAKE + 2) == 4 and _verify(L, am=FAKE + (2 << 34) + 1) == 4
     assert _verify(L, am=FAKE + 64) == 5                 # argmax overlaps logits
     assert _verify(L, acc=FAKE + (2 << 34) + 4) == 5     # accept overlaps argmax
+
+
+def _sample(L, logits=FAKE, guess=FAKE + (1 << 34), uniform=FAKE + (11 << 34), steps=4, n=4, vocab=1000,
+            temperature=0.8, tok=FAKE + (2 << 34), m=FAKE + (3 << 34), acc=FAKE + (4 << 34),
+            col=FAKE + (12 << 34)):
+    return L.pti_verify_sample(logits, guess, uniform, steps, n, vocab, temperature, tok, m, acc, col, None)
+
+
+def test_verify_sample_validation(L):
+    """Every call below fails validation, so nothing is launched."""
+    assert _sample(L, n=0) == 3 and _sample(L, n=5) == 3
+    assert _sample(L, steps=-1) == 2 and _sample(L, vocab=0) == 2 and _sample(L, vocab=1 << 31) == 2
+    for bad in (0.0, -1.0, float("inf"), float("nan"), 1e-45):
+        assert _sample(L, temperature=bad) == 8, bad
+    assert _sample(L, temperature=0.0, steps=0) == 8      # scalars are checked even for no steps
+    assert _sample(L, uniform=None) == 1 and _sample(L, tok=None) == 1 and _sample(L, m=None) == 1
+    assert _sample(L, acc=None) == 1 and _sample(L, logits=None) == 1 and _sample(L, guess=None) == 1
+    assert _sample(L, uniform=FAKE + (11 << 34) + 2) == 4 and _sample(L, col=FAKE + (12 << 34) + 1) == 4
+    assert _sample(L, tok=FAKE + 64) == 5                  # token overlaps logits
+    assert _sample(L, col=FAKE + (11 << 34) + 8) == 5      # collision overlaps uniform
+    assert _sample(L, m=FAKE + (2 << 34) + 8) == 5         # match overlaps token
+    assert _sample(L, acc=FAKE + (12 << 34) + 4) == 5      # accept overlaps collision
 
 
 def _ptrs(*vals):

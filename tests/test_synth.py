@@ -58,3 +58,20 @@ def test_verify_batch_plants_a_unique_maximum():
             assert np.sum(row == row.max()) == 1
             assert row[planted[t, s]] == row.max()
     assert guess.dtype == np.int32 and guess.min() >= 0 and guess.max() < 301
+
+
+def test_uniform_f32_is_on_the_half_open_unit_interval():
+    u = pti_synth.uniform_f32(0, 3, 1 << 20)
+    assert u.dtype == np.float32 and u.min() >= 0.0 and u.max() < 1.0
+    assert np.all(u * np.float32(2 ** 24) == np.floor(u * np.float32(2 ** 24)))   # 24-bit grid
+    assert abs(float(u.astype(np.float64).mean()) - 0.5) < 0.002
+
+
+def test_sample_batch_masks_but_keeps_token_zero():
+    logits, u = pti_synth.sample_batch(6, 4, 500, seed=2, masked=0.9)
+    assert logits.shape == (6, 4, 500) and u.shape == (6, 4)
+    assert np.all(np.isfinite(logits[:, :, 0]))
+    frac = np.isinf(logits).mean()
+    assert 0.85 < frac < 0.95 and np.all(logits[np.isinf(logits)] < 0)
+    plain, u2 = pti_synth.sample_batch(6, 4, 500, seed=2)
+    assert np.array_equal(u, u2) and np.all(np.isfinite(plain))
