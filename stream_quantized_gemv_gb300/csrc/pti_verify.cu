@@ -21,6 +21,7 @@
 #include <cstdint>
 
 #include "pti.h"
+#include "pti_device.cuh"
 #include "pti_host.h"
 
 namespace pti {
@@ -143,24 +144,54 @@ __global__ void __launch_bounds__(kVerifyThreads)
 constexpr int kSampleThreads = 512;
 constexpr int kSampleWarps = kSampleThreads / 32;
 constexpr int kSampleDepth = 4;  // 16-byte loads in flight per lane in pass 1
+constexpr int kSampleBlocksPerSM = 3;  // resident CTAs per SM (40 registers a thread)
 
 struct OnlineSums {
-  float m, s, q;  // running maximum, sum of 2^((x-m)c), sum of its square
+  float m, s, q;  // maximum, sum of 2^((x-m)c), sum of its square
 };
 
-__device__ __forceinline__ void online_add4(OnlineSums &a, const float4 &v, float c) {
+// 2^x by the PTX ISA's ex2.approx.ftz.f32 instruction (a few ulp of relative
+// error).  A result below 2^-126 flushes to zero, which drops only tokens
+// whose probability is below 1e-38 of the most likely one.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// The unnormalised weights e = 2^((x - m) c) of four logits, as two packed
+// pairs; x - m and the product by c are rounded like the scalar operations.
+__device__ __forceinline__ void weights4(const float4 &v, uint64_t neg_m2, uint64_t c2, uint64_t &e01,
+                                         uint64_t &e23) {
+  const float2 a = unpack2(fmul2(fadd2(pack2(v.x, v.y), neg_m2), c2));
+  const float2 b = unpack2(fmul2(fadd2(pack2(v.z, v.w), neg_m2), c2));
+  e01 = pack2(ex2(a.x), ex2(a.y));
+  e23 = pack2(ex2(b.x), ex2(b.y));
+}
+
+// One lane's running sums over its share of a segment, two packed lanes each.
+struct LaneSums {
+  float m;          // running maximum
+  uint64_t neg_m2;  // (-m, -m)
+  uint64_t s2, q2;  // sums of e and of e^2, relative to m
+};
+
+__device__ __forceinline__ void lane_add4(LaneSums &a, const float4 &v, uint64_t c2, float c) {
   const float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
   if (!(mx > -INFINITY)) return;  // four masked tokens (or padding): no mass
   if (mx > a.m) {
-    const float r = exp2f((a.m - mx) * c);  // a.m = -inf gives r = 0
-    a.s *= r;
-    a.q *= r * r;
+    const float r = ex2((a.m - mx) * c);  // a.m = -inf gives r = 0
+    a.s2 = fmul2(a.s2, pack2(r, r));
+    a.q2 = fmul2(a.q2, pack2(r * r, r * r));
     a.m = mx;
+    a.neg_m2 = pack2(-mx, -mx);
   }
-  const float e0 = exp2f((v.x - a.m) * c), e1 = exp2f((v.y - a.m) * c);
-  const float e2 = exp2f((v.z - a.m) * c), e3 = exp2f((v.w - a.m) * c);
-  a.s += (e0 + e1) + (e2 + e3);
-  a.q += (e0 * e0 + e1 * e1) + (e2 * e2 + e3 * e3);
+  uint64_t e01, e23;
+  weights4(v, a.neg_m2, c2, e01, e23);
+  a.s2 = fadd2(a.s2, e01);
+  a.s2 = fadd2(a.s2, e23);
+  a.q2 = ffma2(e01, e01, a.q2);
+  a.q2 = ffma2(e23, e23, a.q2);
 }
 
 __device__ __forceinline__ OnlineSums online_merge(OnlineSums a, OnlineSums b, float c) {
@@ -170,7 +201,7 @@ __device__ __forceinline__ OnlineSums online_merge(OnlineSums a, OnlineSums b, f
     b = t;
   }
   if (!(b.m > -INFINITY)) return a;
-  const float r = exp2f((b.m - a.m) * c);
+  const float r = ex2((b.m - a.m) * c);
   a.s += b.s * r;
   a.q += b.q * (r * r);
   return a;
@@ -190,7 +221,7 @@ __device__ __forceinline__ float4 load4(const float *row, int64_t i, int64_t end
 }
 
 template <bool kVec>
-__global__ void __launch_bounds__(kSampleThreads)
+__global__ void __launch_bounds__(kSampleThreads, kSampleBlocksPerSM)
     verify_sample_kernel(const float *__restrict__ logits, const int32_t *__restrict__ guess,
                          const float *__restrict__ uniform, int64_t steps, int n, int64_t vocab, float c,
                          int32_t *__restrict__ token_out, uint8_t *__restrict__ match_out,
@@ -202,6 +233,7 @@ __global__ void __launch_bounds__(kSampleThreads)
   __shared__ int s_seg;
   __shared__ float s_theta, s_max;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint64_t c2 = pack2(c, c);
   const int64_t seg = ((vocab + 4 * kSampleWarps - 1) / (4 * kSampleWarps)) * 4;
   const int64_t run_len = ((seg + 4 * kSampleThreads - 1) / (4 * kSampleThreads)) * 4;
   for (int64_t t = blockIdx.x; t < steps; t += gridDim.x) {
@@ -209,16 +241,18 @@ __global__ void __launch_bounds__(kSampleThreads)
       const float *row = logits + (t * n + s) * vocab;
       // ---- pass 1: this warp's segment, online maximum and sums
       const int64_t lo = warp * seg, hi = min(lo + seg, vocab);
-      OnlineSums a{-INFINITY, 0.0f, 0.0f};
-      int64_t i = lo + 4 * lane;
-      for (; i + 32 * 4 * (kSampleDepth - 1) < hi; i += 32 * 4 * kSampleDepth) {
+      LaneSums ls{-INFINITY, pack2(INFINITY, INFINITY), 0, 0};
+      // kSampleDepth loads in flight per lane, also in the segment's last
+      // round (positions past its end read as -inf)
+      for (int64_t i = lo + 4 * lane; i < hi; i += 32 * 4 * kSampleDepth) {
         float4 v[kSampleDepth];
 #pragma unroll
         for (int d = 0; d < kSampleDepth; ++d) v[d] = load4<kVec>(row, i + 128 * d, hi);
 #pragma unroll
-        for (int d = 0; d < kSampleDepth; ++d) online_add4(a, v[d], c);
+        for (int d = 0; d < kSampleDepth; ++d) lane_add4(ls, v[d], c2, c);
       }
-      for (; i < hi; i += 128) online_add4(a, load4<kVec>(row, i, hi), c);
+      const float2 s_pair = unpack2(ls.s2), q_pair = unpack2(ls.q2);
+      OnlineSums a{ls.m, s_pair.x + s_pair.y, q_pair.x + q_pair.y};
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         OnlineSums b;
@@ -230,28 +264,43 @@ __global__ void __launch_bounds__(kSampleThreads)
       if (lane == 0) s_warp[warp] = a;
       __syncthreads();
       // ---- row maximum, normaliser, collision; the segment holding the draw
-      if (tid == 0) {
-        float m = -INFINITY;
-        for (int w = 0; w < kSampleWarps; ++w) m = fmaxf(m, s_warp[w].m);
-        float z = 0.0f, q = 0.0f, cum[kSampleWarps];
-        int last_w = 0;
-        for (int w = 0; w < kSampleWarps; ++w) {
-          const float r = (s_warp[w].m > -INFINITY) ? exp2f((s_warp[w].m - m) * c) : 0.0f;
-          const float mass = s_warp[w].s * r;
-          if (mass > 0.0f) last_w = w;
-          z += mass;
-          q += s_warp[w].q * (r * r);
-          cum[w] = z;
+      if (warp == 0) {
+        const OnlineSums w_sums = lane < kSampleWarps ? s_warp[lane] : OnlineSums{-INFINITY, 0.0f, 0.0f};
+        float m = w_sums.m;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        const float r = (w_sums.m > -INFINITY) ? ex2((w_sums.m - m) * c) : 0.0f;
+        float q = w_sums.q * (r * r);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xFFFFFFFFu, q, o);
+        if (lane < kSampleWarps) s_scan[lane] = w_sums.s * r;  // segment masses
+        __syncwarp();
+        if (lane == 0) {
+          float z = 0.0f;
+          int last_w = 0;
+          for (int w = 0; w < kSampleWarps; ++w) {
+            z += s_scan[w];
+            if (s_scan[w] > 0.0f) last_w = w;
+          }
+          if (collision_out != nullptr) collision_out[t * n + s] = q / (z * z);
+          const float theta = uniform[t * n + s] * z;
+          // the first segment whose running mass passes theta (the running sum
+          // repeats the one above term by term)
+          float cum = 0.0f, below = 0.0f;
+          int w = 0;
+          for (; w < kSampleWarps; ++w) {
+            below = cum;
+            cum += s_scan[w];
+            if (cum > theta) break;
+          }
+          s_seg = w < kSampleWarps ? w : last_w;
+          // mass left to pass within the segment (>= 0); when u Z lies at the
+          // end of the row within rounding, no run may claim and the draw is
+          // the last token with mass
+          s_theta = w < kSampleWarps ? theta - below : INFINITY;
+          s_max = m;
+          s_tok[s] = INT_MAX;
         }
-        if (collision_out != nullptr) collision_out[t * n + s] = q / (z * z);
-        const float theta = uniform[t * n + s] * z;
-        int w = 0;
-        while (w < kSampleWarps && !(cum[w] > theta)) ++w;
-        if (w == kSampleWarps) w = last_w;  // u Z at the end of the row within rounding
-        s_seg = w;
-        s_theta = theta - (w > 0 ? cum[w - 1] : 0.0f);  // >= 0: mass left to pass in the segment
-        s_max = m;
-        s_tok[s] = INT_MAX;
       }
       __syncthreads();
       // ---- pass 2: the draw's segment again, thread k taking the k-th run of
@@ -259,19 +308,26 @@ __global__ void __launch_bounds__(kSampleThreads)
       // that thread walks its run once more
       const int64_t slo = s_seg * seg, shi = min(slo + seg, vocab);
       const int64_t jlo = slo + tid * run_len, jhi = min(jlo + run_len, shi);
-      const float m = s_max, theta = s_theta;
+      const float theta = s_theta;
+      const uint64_t neg_m2 = pack2(-s_max, -s_max);
       float own = 0.0f;
       int last = -1;  // last token of the run with mass (the rounding fallback)
-#pragma unroll 4
-      for (int64_t j = jlo; j < jhi; j += 4) {
-        const float4 v = load4<kVec>(row, j, jhi);
-        const float e0 = exp2f((v.x - m) * c), e1 = exp2f((v.y - m) * c);
-        const float e2 = exp2f((v.z - m) * c), e3 = exp2f((v.w - m) * c);
-        own += (e0 + e1) + (e2 + e3);
-        if (e3 > 0.0f) last = static_cast<int>(j + 3);
-        else if (e2 > 0.0f) last = static_cast<int>(j + 2);
-        else if (e1 > 0.0f) last = static_cast<int>(j + 1);
-        else if (e0 > 0.0f) last = static_cast<int>(j);
+      for (int64_t j0 = jlo; j0 < jhi; j0 += 4 * kSampleDepth) {
+        float4 v[kSampleDepth];
+#pragma unroll
+        for (int d = 0; d < kSampleDepth; ++d) v[d] = load4<kVec>(row, j0 + 4 * d, jhi);
+#pragma unroll
+        for (int d = 0; d < kSampleDepth; ++d) {
+          const int64_t j = j0 + 4 * d;
+          uint64_t e01, e23;
+          weights4(v[d], neg_m2, c2, e01, e23);
+          const float2 a01 = unpack2(e01), a23 = unpack2(e23);
+          own += (a01.x + a01.y) + (a23.x + a23.y);
+          if (a23.y > 0.0f) last = static_cast<int>(j + 3);
+          else if (a23.x > 0.0f) last = static_cast<int>(j + 2);
+          else if (a01.y > 0.0f) last = static_cast<int>(j + 1);
+          else if (a01.x > 0.0f) last = static_cast<int>(j);
+        }
       }
       float incl = own;
 #pragma unroll
@@ -300,9 +356,10 @@ __global__ void __launch_bounds__(kSampleThreads)
         float cum = before + prev;
         int k = -1;
         for (int64_t j = jlo; j < jhi && k < 0; j += 4) {
-          const float4 v = load4<kVec>(row, j, jhi);
-          const float e[4] = {exp2f((v.x - m) * c), exp2f((v.y - m) * c), exp2f((v.z - m) * c),
-                              exp2f((v.w - m) * c)};
+          uint64_t e01, e23;
+          weights4(load4<kVec>(row, j, jhi), neg_m2, c2, e01, e23);
+          const float2 a01 = unpack2(e01), a23 = unpack2(e23);
+          const float e[4] = {a01.x, a01.y, a23.x, a23.y};
           for (int d = 0; d < 4 && k < 0; ++d) {
             cum += e[d];
             if (cum > theta && e[d] > 0.0f) k = static_cast<int>(j + d);
@@ -410,13 +467,14 @@ extern "C" pti_status pti_verify_sample(const float *logits, const int32_t *gues
   }
   const int sms = current_device_sms();
   if (sms <= 0) return PTI_ERR_CUDA;
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(steps, static_cast<int64_t>(sms) * 4));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (aligned(logits, 16) && vocab % 4 == 0)
-    verify_sample_kernel<true><<<grid, kSampleThreads, 0, st>>>(logits, guess, uniform, steps, n_streams, vocab, c,
-                                                                token_out, match_out, accept_len_out, collision_out);
-  else
-    verify_sample_kernel<false><<<grid, kSampleThreads, 0, st>>>(logits, guess, uniform, steps, n_streams, vocab, c,
-                                                                 token_out, match_out, accept_len_out, collision_out);
+  const bool vec = aligned(logits, 16) && vocab % 4 == 0;
+  auto kernel = vec ? verify_sample_kernel<true> : verify_sample_kernel<false>;
+  // one wave of resident CTAs, each taking every grid-th step
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kSampleThreads, 0) != cudaSuccess || per_sm < 1)
+    return PTI_ERR_CUDA;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(steps, static_cast<int64_t>(sms) * per_sm));
+  kernel<<<grid, kSampleThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      logits, guess, uniform, steps, n_streams, vocab, c, token_out, match_out, accept_len_out, collision_out);
   return launch_status();
 }
