@@ -49,25 +49,32 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+GEMV_SOURCES = ("pti_gemv_kernel.cuh", "pti_gemv.cu", "pti_device.cuh", "pti_host.h")
+DECODE_SOURCES = GEMV_SOURCES + ("pti_decode.cu",)
+VERIFY_SOURCES = ("pti_verify.cu", "pti_device.cuh", "pti_host.h")
+
+
+def kernel_source_hash(files) -> str:
+    """Hash of the CUDA sources a workload's kernels are built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "stream_quantized_gemv_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(files):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, if it was taken on the current kernel sources; else None."""
+def recorded_traffic(wl):
+    """DRAM bytes per launch of the workload's dominant kernel from the
+    committed ncu summary, if it was taken on the current kernel sources;
+    else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        e = d.get(workload)
-        if e and e.get("kernel_source_hash") == kernel_source_hash():
+        e = d.get(wl.name)
+        if e and e.get("kernel_source_hash") == kernel_source_hash(wl.sources):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -166,6 +173,7 @@ TWIN_BLOCK = 68
 
 class Q8Pass:
     """N-stream Q8 GEMV over L distinct rows x cols matrices (one step = one pass)."""
+    sources = GEMV_SOURCES
 
     def __init__(self, rows=17408, cols=5120, n=4, layers=16, seed=0):
         import torch
@@ -285,6 +293,8 @@ class TwinPass(Q8Pass):
 
 
 class VerifyBatch(Q8Pass):
+    sources = VERIFY_SOURCES
+
     def __init__(self, steps=4096, n=4, vocab=151936, p=0.6, seed=0):
         import torch
         import pti_synth
@@ -328,6 +338,7 @@ class VerifyBatch(Q8Pass):
 class VerifySampleBatch(Q8Pass):
     """Sampling-mode verify of a batch: inverse-CDF draws from softmax(l / T)
     per stream, acceptance against guesses and sum p^2 (one step = one batch)."""
+    sources = VERIFY_SOURCES
 
     def __init__(self, steps=4096, n=4, vocab=151936, temperature=1.0, seed=0):
         import torch
@@ -447,8 +458,8 @@ WORKLOADS = {
     "q8": lambda a: Q8Pass(a.rows or 17408, a.cols or 5120, a.n, a.layers or 16),
     "twin": lambda a: TwinPass(a.rows or 17408, a.cols or 5120, a.layers or 8),
     "twin2": lambda a: TwinPass(a.rows or 17408, a.cols or 5120, a.layers or 8, per_model=2),
-    "verify": lambda a: VerifyBatch(),
-    "verify_sample": lambda a: VerifySampleBatch(),
+    "verify": lambda a: VerifyBatch(steps=a.vsteps),
+    "verify_sample": lambda a: VerifySampleBatch(steps=a.vsteps),
 }
 
 
@@ -557,6 +568,7 @@ def main():
     ap.add_argument("--rows", type=int, default=0)
     ap.add_argument("--cols", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--vsteps", type=int, default=4096, help="steps of the verify batches")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
@@ -604,7 +616,7 @@ def main():
         value = wl.step_bytes * world / (ms * 1e-3) / 1e9
         per_launch_ms = ms / getattr(wl, "gemv_launches_per_step", wl.launches_per_step)
         achieved = wl.launch_bytes / (per_launch_ms * 1e-3) / 1e9
-        traffic = recorded_traffic(wl.name)
+        traffic = recorded_traffic(wl)
         line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
                 "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 5),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -657,10 +669,10 @@ def _cpu_only_workload(name, a):
         wl.rows, wl.cols, wl.n, wl.layers = a.rows or 17408, a.cols or 5120, 2 * wl.per_model, a.layers or 8
         wl.weight_bytes = wl.rows * (wl.cols // 32) * TWIN_BLOCK
     elif name == "verify_sample":
-        wl.steps, wl.n, wl.vocab, wl.temperature = 4096, 4, 151936, 1.0
+        wl.steps, wl.n, wl.vocab, wl.temperature = a.vsteps, 4, 151936, 1.0
         wl.launch_bytes = wl.steps * wl.n * wl.vocab * 4
     else:
-        wl.steps, wl.n, wl.vocab, wl.p = 4096, 4, 151936, 0.6
+        wl.steps, wl.n, wl.vocab, wl.p = a.vsteps, 4, 151936, 0.6
         wl.launch_bytes = wl.steps * wl.n * wl.vocab * 4
     return wl
 
