@@ -441,7 +441,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // Warp s < kOut handles vector s; must run after the wait on the previous
 // kernel.  A consumer barrier must separate it from the first reader.
 template <int kOut>
-__device__ __noinline__ void input_scales(const GemvArgs &a, uint32_t warp, uint32_t lane, float *scale) {
+__device__ __forceinline__ void input_scales_body(const GemvArgs &a, uint32_t warp, uint32_t lane, float *scale) {
   if (warp >= static_cast<uint32_t>(kOut)) return;
   double s2 = 0.0;
   if (a.sq_in != nullptr) {
@@ -452,6 +452,13 @@ __device__ __noinline__ void input_scales(const GemvArgs &a, uint32_t warp, uint
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xFFFFFFFFu, s2, o);
   if (lane == 0) scale[warp] = a.sq_in != nullptr ? static_cast<float>(1.0 / sqrt(s2 * a.inv_len_in + a.eps)) : 1.0f;
+}
+
+// Out of line for the GEMV's consumers (one shared copy keeps their
+// instruction footprint small).
+template <int kOut>
+__device__ __noinline__ void input_scales(const GemvArgs &a, uint32_t warp, uint32_t lane, float *scale) {
+  input_scales_body<kOut>(a, warp, lane, scale);
 }
 
 // Decode-pass epilogue of gate/up tile rb: the tile's rows 0..63 are gate rows
@@ -515,18 +522,34 @@ __device__ __forceinline__ int red_warp(int q, int h) {
 }
 
 // Total of element (s, row) of shared tile rb: the partials of its CTAs
-// c_lo .. c_hi added in CTA order (each CTA's slot: 0 if rb is its first
-// tile, else 1), so the result does not depend on which CTA adds them.
+// c_lo .. c_hi added in CTA order, so the result does not depend on which CTA
+// or kernel adds them.  Each CTA's partial sits in slot 0 if rb is its first
+// tile, else slot 1: the CTAs after c_lo start inside tile rb, so only c_lo
+// can hold it in slot 1 (`lo_slot`).  The loads of up to kPartialBatch
+// contributors are issued together.
+constexpr int kPartialBatch = 8;
+
 template <int kOut>
-__device__ __forceinline__ float sum_partials(const GemvArgs &a, int32_t rb, int32_t c_lo, int32_t c_hi, int s,
+__device__ __forceinline__ float sum_partials(const GemvArgs &a, int32_t c_lo, int32_t c_hi, int lo_slot, int s,
                                               int row) {
   float total = 0.0f;
-  for (int32_t c = c_lo; c <= c_hi; ++c) {
-    const int cs = (rb == first_tile_of_cta(c, a.units, a.grid, a.n_sb)) ? 0 : 1;
-    const float v = __ldcg(&a.part[((static_cast<int64_t>(c) * 2 + cs) * kOut + s) * kRowsPerTile + row]);
-    total = (c == c_lo) ? v : total + v;
+  for (int32_t c0 = c_lo; c0 <= c_hi; c0 += kPartialBatch) {
+    float v[kPartialBatch];
+#pragma unroll
+    for (int k = 0; k < kPartialBatch; ++k) {
+      const int32_t c = c0 + k;
+      const int cs = c == c_lo ? lo_slot : 0;
+      v[k] = c <= c_hi ? __ldcg(&a.part[((static_cast<int64_t>(c) * 2 + cs) * kOut + s) * kRowsPerTile + row]) : 0.0f;
+    }
+#pragma unroll
+    for (int k = 0; k < kPartialBatch; ++k)
+      if (c0 + k <= c_hi) total = (c0 + k == c_lo) ? v[k] : total + v[k];
   }
   return total;
+}
+
+__device__ __forceinline__ int partial_slot_of_first(int32_t rb, int32_t c_lo, const GemvArgs &a) {
+  return rb == first_tile_of_cta(c_lo, a.units, a.grid, a.n_sb) ? 0 : 1;
 }
 
 // Writes element (s, row) of tile rb: y for Plain, else the epilogue's tile
@@ -627,7 +650,9 @@ __device__ __noinline__ void finish_tiles(const GemvArgs &a, const float *red, i
       if (epilogue_ran) named_barrier(kBarConsumers, kConsumerThreads);  // tile_out and wsum are reused
     for (int t = tid; t < kOut * kRowsPerTile; t += kConsumerThreads) {
       const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
-      const float total = shared_tile ? sum_partials<kOut>(a, rbs[k], clo[k], chi[k], s, row) : warp_total(k, s, row);
+      const float total =
+          shared_tile ? sum_partials<kOut>(a, clo[k], chi[k], partial_slot_of_first(rbs[k], clo[k], a), s, row)
+                      : warp_total(k, s, row);
       deliver<F, N, E>(a, epi, rbs[k], s, row, total);
     }
     if constexpr (E != Epi::Plain) {
@@ -641,26 +666,31 @@ __device__ __noinline__ void finish_tiles(const GemvArgs &a, const float *red, i
 // Adds the partials of the shared row tiles of a GEMV launch (one CTA per
 // row tile; tiles a single CTA computed were written by the GEMV) and runs
 // the fused epilogue on them.  Launched right after the GEMV with
-// programmatic dependent launch: it is resident early and waits for the GEMV
-// to complete.
+// programmatic dependent launch: it is resident early, works out which CTAs
+// share its tile (CTAs of unshared tiles exit at once) and only then waits
+// for the GEMV; after the wait every load it needs (the partials, the input's
+// sums of squares) is issued before the first is used.
 constexpr int kCombineThreads = 512;
 
 template <Fmt F, int N, Epi E>
 __global__ void __launch_bounds__(kCombineThreads) combine_tiles_kernel(const __grid_constant__ GemvArgs a) {
   constexpr int kOut = Traits<F, N>::kOut;
+  static_assert(kOut * kRowsPerTile <= kCombineThreads, "one element per thread");
   __shared__ float epi[kEpiBytes / 4];
   const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
   pdl_launch_dependents();
-  pdl_wait_primary();
   const int32_t rb = static_cast<int32_t>(blockIdx.x);
   const int32_t c_lo = cta_of_unit(static_cast<int64_t>(rb) * a.n_sb, a.units, a.grid);
   const int32_t c_hi = cta_of_unit(static_cast<int64_t>(rb + 1) * a.n_sb - 1, a.units, a.grid);
   if (c_hi == c_lo) return;  // written by the GEMV
-  if constexpr (E != Epi::Plain) input_scales<kOut>(a, warp, lane, epi + 4 * kRowsPerTile);
-  for (int t = tid; t < kOut * kRowsPerTile; t += kCombineThreads) {
-    const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
-    deliver<F, N, E>(a, epi, rb, s, row, sum_partials<kOut>(a, rb, c_lo, c_hi, s, row));
-  }
+  const int lo_slot = partial_slot_of_first(rb, c_lo, a);
+  const int t = static_cast<int>(tid);
+  const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
+  pdl_wait_primary();
+  float total = 0.0f;
+  if (t < kOut * kRowsPerTile) total = sum_partials<kOut>(a, c_lo, c_hi, lo_slot, s, row);
+  if constexpr (E != Epi::Plain) input_scales_body<kOut>(a, warp, lane, epi + 4 * kRowsPerTile);
+  if (t < kOut * kRowsPerTile) deliver<F, N, E>(a, epi, rb, s, row, total);
   if constexpr (E != Epi::Plain) {
     named_barrier(kBarConsumers, kCombineThreads);
     run_epilogue<kOut, E>(a, epi, rb, tid, kCombineThreads);
