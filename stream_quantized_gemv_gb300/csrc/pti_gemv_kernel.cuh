@@ -17,19 +17,19 @@
 //    (box 34 x 8 bytes by 128 rows) brings a unit into shared memory.
 //  * Persistent grid, one CTA per SM, stream-K split: CTA c owns the units
 //    [c U / G, (c+1) U / G) in row-major order, so every SM streams the same
-//    number of bytes.  Row tiles shared by several CTAs are combined by the
-//    last CTA to finish them (an atomic ticket per tile, partials in a
-//    caller-supplied workspace, summed in a fixed CTA order).
+//    number of bytes.  Row tiles shared by several CTAs are combined by a
+//    small kernel launched right behind the GEMV (partials in a
+//    caller-supplied workspace, summed in a fixed CTA order); the persistent
+//    decode kernel instead lets the last CTA to finish a tile combine it (an
+//    atomic ticket per tile).
 //  * Lane 0 of consumer warp 0 issues the copies into a ring of up to 6 stages
 //    guarded by mbarriers (it refills a slot once every warp has released
 //    it); 16 warps compute.  Q8: warp w always computes block w % 8 of each
-//    unit for 64 rows (two per lane), reading each row's 48-byte window around
-//    the block with three aligned, conflict-free 16-byte loads; the four warps
-//    of a scheduler share one code body.  Twin: lane l of a task owns two rows
-//    and reads its 16-byte chunk of each; the 17 chunk positions fall into a
-//    few structural classes (where the block scale sits in the chunk), one
-//    code body per class; scheduler k owns chunks k, k+4, k+8, k+12 (chunk 16
-//    rotates over the schedulers from unit to unit).
+//    unit for 64 rows (two per lane), reading each row's 40-byte window around
+//    the block with five aligned 8-byte loads; the four warps of a scheduler
+//    share one code body.  Twin: warp w computes half of block w % 4 (16
+//    columns of both models) of each unit for 64 rows, two per lane; the
+//    block is fixed per scheduler, so its byte offsets are compile-time.
 //  * Each stage also holds the unit's slice of the activations (N x 1 KB,
 //    stream-major), fetched by one bulk copy per stream next to the weight
 //    tile.  Every warp reads them with broadcast loads and reuses them for its
@@ -37,9 +37,11 @@
 //    with the number of rows (the L2 thrash the pages diagnose for the
 //    per-row-block design comes from re-reading x once per row block).
 //  * Dequantisation is exact (see pti_device.cuh); products use packed
-//    f32x2 FMAs.  Each chunk's products are summed into a fresh partial, which
-//    is then added to the running accumulator, so no fp32 chain is longer than
-//    a few dozen dependent roundings per output.
+//    f32x2 FMAs.  A warp's products of one unit are summed into a fresh
+//    partial (16 Q8 or 8 twin products per half of the pair), which is then
+//    added to the running accumulator once per super-block, so an output's
+//    longest chain of dependent roundings is about K/256 (Q8) or K/128 (twin)
+//    plus a few dozen.
 //  * Programmatic dependent launch: the producer fetches its first weight
 //    tiles before waiting for the previous kernel in the stream, and only then
 //    fetches activations; nothing is written before that wait.
@@ -137,192 +139,21 @@ struct GemvArgs {
   int32_t combine_in_kernel;  // 1: tickets and the last CTA combine shared tiles; 0: combine_tiles_kernel does
 };
 
-// Rows handled by one warp task: lane l owns rows 64h + l and 64h + 32 + l of
-// the tile (h = the task's half).  (Four rows per lane halves the activation
-// loads per weight but doubles the code of each chunk body; measured slower.)
+// Rows handled by one consumer warp: lane l owns rows 64h + l and 64h + 32 + l
+// of the tile (h = the warp's half).  (Four rows per lane halves the
+// activation loads per weight but needs 8 instead of 16 warps per tile within
+// the register budget; measured slower.)
 constexpr int kTaskSlots = 2;
 
-// Where a 16-byte chunk's weights sit.  Chunks come in a few structural
-// classes: `cls` = -1 when the chunk holds no scale (all its bytes are weights
-// of block b0), else the index of the byte pair holding the next block's scale
-// (Q8: 0..7; twin: the word index 0..3).  The generic parameters are the byte
-// offset of the chunk, the offset of block b0's scale in the row, and the
-// column pair of the chunk's first weight pair (`cpbase`).
-struct ChunkParams {
-  int cls;
-  uint32_t choff;     // 16 * c
-  uint32_t scale_off; // byte offset of block b0's scale within the super-block row
-  uint32_t cpbase;    // column pair (within the super-block) of pair 0
-};
-
-__device__ __forceinline__ ChunkParams q8_chunk_params(int c) {
-  ChunkParams p;
-  p.choff = 16u * c;
-  if (c <= 14 && (c & 1) == 0) {  // the scale of block c/2 sits at pair (16c - 34(c/2)) / 2 = c/2
-    p.cls = c / 2;
-    const int b0 = c / 2 > 0 ? c / 2 - 1 : 0;
-    p.scale_off = 34u * b0;
-    p.cpbase = 15u * (c / 2);
-  } else {
-    const int b0 = (16 * c) / 34;
-    p.cls = -1;
-    p.scale_off = 34u * b0;
-    p.cpbase = static_cast<uint32_t>((32 * b0 + (16 * c) % 34 - 2) / 2);
-  }
-  return p;
-}
-
-__device__ __forceinline__ ChunkParams twin_chunk_params(int c) {
-  ChunkParams p;
-  p.choff = 16u * c;
-  if ((c & 3) == 0 && c <= 12) {  // chunk c holds the scale word of block c/4 at word c/4
-    p.cls = c / 4;
-    const int b0 = c / 4 > 0 ? c / 4 - 1 : 0;
-    p.scale_off = 68u * b0;
-    p.cpbase = 15u * (c / 4);
-  } else {
-    const int b0 = (4 * c) / 17;
-    p.cls = -1;
-    p.scale_off = 68u * b0;
-    p.cpbase = static_cast<uint32_t>(16 * b0 + (4 * c) % 17 - 1);
-  }
-  return p;
-}
-
-template <int I>
-__device__ __forceinline__ uint32_t word_at(const uint4 &w) {
-  if constexpr (I == 0) return w.x;
-  else if constexpr (I == 1) return w.y;
-  else if constexpr (I == 2) return w.z;
-  else return w.w;
-}
-
-// One Q8 chunk of class K for the lane's two rows of half h.  Byte pair m of
-// the chunk holds weight columns cpbase + m (pairs before the scale) or
-// cpbase + m - 1 (pairs after it).
-template <int N, int K>
-__device__ __forceinline__ void q8_body(const uint8_t *tile, const ChunkParams &cp, const uint8_t *xsb,
-                                        uint32_t lane, uint32_t half, uint64_t (&acc)[kTaskSlots][N]) {
-  constexpr int M0 = (K == 0) ? 1 : 0;  // first weight pair
-  uint32_t wx[kTaskSlots][4];
-  ScalePair s_lo[kTaskSlots], s_hi[kTaskSlots];
-#pragma unroll
-  for (int r = 0; r < kTaskSlots; ++r) {
-    const uint8_t *row = tile + (half * 64 + r * 32 + lane) * kSBBytes;
-    const uint4 w = *reinterpret_cast<const uint4 *>(row + cp.choff);
-    if constexpr (K != 0) s_lo[r] = make_scale(*reinterpret_cast<const uint16_t *>(row + cp.scale_off));
-    if constexpr (K >= 0) {
-      const uint32_t wd = word_at<K / 2>(w);
-      s_hi[r] = make_scale((K & 1) ? (wd >> 16) : (wd & 0xFFFFu));
-    }
-    wx[r][0] = w.x ^ 0x80808080u;
-    wx[r][1] = w.y ^ 0x80808080u;
-    wx[r][2] = w.z ^ 0x80808080u;
-    wx[r][3] = w.w ^ 0x80808080u;
-  }
-  const uint8_t *xc = xsb + cp.cpbase * 8;
-  uint64_t p[kTaskSlots][N];
-  static_for<0, 8>([&](auto mc) {
-    constexpr int m = decltype(mc)::value;
-    if constexpr (m != K) {
-      constexpr int off = (K >= 0 && m > K) ? m - 1 : m;
-      uint64_t xv[N];
-#pragma unroll
-      for (int st = 0; st < N; ++st)
-        xv[st] = *reinterpret_cast<const uint64_t *>(xc + st * Stage<Fmt::Q8, N>::kXStreamBytes + off * 8);
-#pragma unroll
-      for (int r = 0; r < kTaskSlots; ++r) {
-        const ScalePair &sc = (K < 0 || m < K) ? s_lo[r] : s_hi[r];
-        const uint64_t wq = dequant2(wx[r][m / 2], (2 * m) % 4, wx[r][m / 2], (2 * m) % 4 + 1, sc);
-        static_for<0, N>([&](auto sc_) {
-          constexpr int s = decltype(sc_)::value;
-          if constexpr (m == M0) p[r][s] = fmul2(wq, xv[s]);
-          else p[r][s] = ffma2(wq, xv[s], p[r][s]);
-        });
-      }
-    }
-  });
-#pragma unroll
-  for (int r = 0; r < kTaskSlots; ++r)
-    static_for<0, N>([&](auto sc_) {
-      constexpr int s = decltype(sc_)::value;
-      acc[r][s] = fadd2(acc[r][s], p[r][s]);
-    });
-}
-
-// One twin chunk of class J for the lane's two rows of half h.  Word j of the
-// chunk holds column pair cpbase + j (before the scale word) or cpbase + j - 1.
-template <int N, int J>
-__device__ __forceinline__ void twin_body(const uint8_t *tile, const ChunkParams &cp, const uint8_t *xsb,
-                                          uint32_t lane, uint32_t half, uint64_t (&acc)[kTaskSlots][2 * N]) {
-  constexpr int J0 = (J == 0) ? 1 : 0;
-  uint4 w[kTaskSlots];
-  ScalePair sa_lo[kTaskSlots], sb_lo[kTaskSlots], sa_hi[kTaskSlots], sb_hi[kTaskSlots];
-#pragma unroll
-  for (int r = 0; r < kTaskSlots; ++r) {
-    const uint8_t *row = tile + (half * 64 + r * 32 + lane) * kSBBytes;
-    w[r] = *reinterpret_cast<const uint4 *>(row + cp.choff);
-    if constexpr (J != 0) {
-      const uint32_t sw = *reinterpret_cast<const uint32_t *>(row + cp.scale_off);
-      sa_lo[r] = make_scale(sw & 0xFFFFu);
-      sb_lo[r] = make_scale(sw >> 16);
-    }
-    if constexpr (J >= 0) {
-      const uint32_t sw = word_at<J>(w[r]);
-      sa_hi[r] = make_scale(sw & 0xFFFFu);
-      sb_hi[r] = make_scale(sw >> 16);
-    }
-  }
-  const uint8_t *xc = xsb + cp.cpbase * 8;
-  uint64_t pa[kTaskSlots][N], pb[kTaskSlots][N];
-  static_for<0, 4>([&](auto jc) {
-    constexpr int j = decltype(jc)::value;
-    if constexpr (j != J) {
-      constexpr int off = (J >= 0 && j > J) ? j - 1 : j;
-      uint64_t xa[N], xb[N];
-#pragma unroll
-      for (int s = 0; s < N; ++s) {
-        xa[s] = *reinterpret_cast<const uint64_t *>(xc + s * Stage<Fmt::Twin, N>::kXStreamBytes + off * 8);
-        xb[s] = *reinterpret_cast<const uint64_t *>(xc + (N + s) * Stage<Fmt::Twin, N>::kXStreamBytes + off * 8);
-      }
-      constexpr bool lo = (J < 0 || j < J);
-#pragma unroll
-      for (int r = 0; r < kTaskSlots; ++r) {
-        const uint32_t wxj = word_at<j>(w[r]) ^ 0x80808080u;
-        const uint64_t wa = dequant2(wxj, 1, wxj, 3, lo ? sa_lo[r] : sa_hi[r]);  // model A: high bytes
-        const uint64_t wb = dequant2(wxj, 0, wxj, 2, lo ? sb_lo[r] : sb_hi[r]);  // model B: low bytes
-#pragma unroll
-        for (int s = 0; s < N; ++s) {
-          if constexpr (j == J0) {
-            pa[r][s] = fmul2(wa, xa[s]);
-            pb[r][s] = fmul2(wb, xb[s]);
-          } else {
-            pa[r][s] = ffma2(wa, xa[s], pa[r][s]);
-            pb[r][s] = ffma2(wb, xb[s], pb[r][s]);
-          }
-        }
-      }
-    }
-  });
-#pragma unroll
-  for (int r = 0; r < kTaskSlots; ++r)
-#pragma unroll
-    for (int s = 0; s < N; ++s) {
-      acc[r][s] = fadd2(acc[r][s], pa[r][s]);
-      acc[r][N + s] = fadd2(acc[r][N + s], pb[r][s]);
-    }
-}
-
 // One Q8 block b of the super-block (columns 32b .. 32b+31) for the lane's
-// two rows of half h.  The block's 34 bytes lie in the 48-byte window that
-// starts at byte 32b of the row (three aligned 16-byte loads, conflict-free
-// since rows are 272 bytes apart), from window byte 2b on.  With b = 2c + e,
-// the block starts in window word c at half-word e: the words c .. c+8 are
-// moved to the front by two selects on c (b is fixed per warp, so the
-// predicates are loop-invariant), after which only the parity e decides where
-// each byte sits: the scale is half-word e of word 0, weight pair j (columns
-// 32b+2j, 32b+2j+1) is at byte 2e+2+2j.  One code body per parity keeps the
-// instruction footprint of all warps small.
+// two rows of half h.  The block's 34 bytes start at byte 34b = 32b + 2b of
+// the row.  With b = 2c + e, the 40-byte window that starts at byte
+// 32b + 8 (c >= 2) of the row (five aligned 8-byte loads; b is fixed per warp,
+// so the offset is loop-invariant) holds the block from word c % 2 on, at
+// half-word e: the scale is half-word e of that word, weight pair j (columns
+// 32b+2j, 32b+2j+1) is at byte 2e+2+2j.  The warps of a scheduler share
+// c % 2 and e, so they run one code body.  (Five 8-byte loads replace three
+// 16-byte loads and ten selects: measured 5% faster at N = 4, 7% at N = 1.)
 template <int N, int E, int CLO>
 __device__ __forceinline__ void q8_block_body(const uint8_t *tile, const uint8_t *xblk, uint32_t lane, uint32_t half,
                                               uint32_t win_off, bool c_hi, uint64_t (&acc)[kTaskSlots][N]) {
@@ -330,14 +161,14 @@ __device__ __forceinline__ void q8_block_body(const uint8_t *tile, const uint8_t
   ScalePair sc[kTaskSlots];
 #pragma unroll
   for (int r = 0; r < kTaskSlots; ++r) {
-    const uint8_t *win = tile + (half * 64 + r * 32 + lane) * kSBBytes + win_off;
-    const uint4 v0 = *reinterpret_cast<const uint4 *>(win);
-    const uint4 v1 = *reinterpret_cast<const uint4 *>(win + 16);
-    const uint4 v2 = *reinterpret_cast<const uint4 *>(win + 32);
-    const uint32_t words[12] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w, v2.x, v2.y, v2.z, v2.w};
+    const uint8_t *win = tile + (half * 64 + r * 32 + lane) * kSBBytes + win_off + (c_hi ? 8u : 0u);
     uint32_t t1[10];
 #pragma unroll
-    for (int k = 0; k < 10; ++k) t1[k] = c_hi ? words[k + 2] : words[k];
+    for (int k = 0; k < 5; ++k) {
+      const uint2 v = *reinterpret_cast<const uint2 *>(win + 8 * k);
+      t1[2 * k] = v.x;
+      t1[2 * k + 1] = v.y;
+    }
 #pragma unroll
     for (int k = 0; k < 9; ++k) w[r][k] = t1[k + CLO];
     sc[r] = make_scale(E ? (w[r][0] >> 16) : (w[r][0] & 0xFFFFu));
@@ -374,37 +205,81 @@ __device__ __forceinline__ void q8_block_body(const uint8_t *tile, const uint8_t
     });
 }
 
-template <Fmt F, int N>
-__device__ __forceinline__ ChunkParams chunk_params(int c) {
-  if constexpr (F == Fmt::Q8) return q8_chunk_params(c);
-  else return twin_chunk_params(c);
-}
-
-template <Fmt F, int N>
-__device__ __forceinline__ void run_chunk(const ChunkParams &cp, const uint8_t *tile, const uint8_t *xsb,
-                                          uint32_t lane, uint32_t half,
-                                          uint64_t (&acc)[kTaskSlots][Traits<F, N>::kOut]) {
-  if constexpr (F == Fmt::Q8) {
-    switch (cp.cls) {
-      case -1: q8_body<N, -1>(tile, cp, xsb, lane, half, acc); break;
-      case 0: q8_body<N, 0>(tile, cp, xsb, lane, half, acc); break;
-      case 1: q8_body<N, 1>(tile, cp, xsb, lane, half, acc); break;
-      case 2: q8_body<N, 2>(tile, cp, xsb, lane, half, acc); break;
-      case 3: q8_body<N, 3>(tile, cp, xsb, lane, half, acc); break;
-      case 4: q8_body<N, 4>(tile, cp, xsb, lane, half, acc); break;
-      case 5: q8_body<N, 5>(tile, cp, xsb, lane, half, acc); break;
-      case 6: q8_body<N, 6>(tile, cp, xsb, lane, half, acc); break;
-      default: q8_body<N, 7>(tile, cp, xsb, lane, half, acc); break;
+// One twin block b of the super-block (columns 32b .. 32b+31, bytes
+// 68b .. 68b+67 of each row) for the lane's two rows of half h, columns
+// 16ch .. 16ch+15 of the block.  The block's scale word (binary16 scale of A,
+// then of B) is at byte 68b; payload word k (columns 2k, 2k+1) at
+// 68b + 4 + 4k holds the bytes [B(2k), A(2k), B(2k+1), A(2k+1)] (each uint16
+// is A << 8 | B, stored little-endian).  The warp's eight payload words start
+// (68b + 4) % 16 bytes past a 16-byte boundary: two or three aligned 16-byte
+// loads, with b (= the warp's scheduler) a compile-time constant, plus one
+// 4-byte load of the scales.
+template <int N, int B>
+__device__ __forceinline__ void twin_block_body(const uint8_t *tile, const uint8_t *xsb, uint32_t lane,
+                                                uint32_t half, uint32_t ch, uint64_t (&acc)[kTaskSlots][2 * N]) {
+  constexpr int kP = (68 * B + 4) % 16;         // payload offset past the 16-byte boundary
+  constexpr int kChunks = (kP + 32 + 15) / 16;  // 16-byte loads covering the 32 payload bytes
+  constexpr int kXS = Stage<Fmt::Twin, N>::kXStreamBytes;
+  uint32_t w[kTaskSlots][8];
+  ScalePair sa[kTaskSlots], sb[kTaskSlots];
+#pragma unroll
+  for (int r = 0; r < kTaskSlots; ++r) {
+    const uint8_t *row = tile + (half * 64 + r * 32 + lane) * kSBBytes;
+    const uint32_t scales = *reinterpret_cast<const uint32_t *>(row + 68 * B);
+    const uint8_t *pl = row + (68 * B + 4 - kP) + 32 * ch;
+    uint32_t words[4 * kChunks];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(pl + 16 * c);
+      words[4 * c] = v.x;
+      words[4 * c + 1] = v.y;
+      words[4 * c + 2] = v.z;
+      words[4 * c + 3] = v.w;
     }
-  } else {
-    switch (cp.cls) {
-      case -1: twin_body<N, -1>(tile, cp, xsb, lane, half, acc); break;
-      case 0: twin_body<N, 0>(tile, cp, xsb, lane, half, acc); break;
-      case 1: twin_body<N, 1>(tile, cp, xsb, lane, half, acc); break;
-      case 2: twin_body<N, 2>(tile, cp, xsb, lane, half, acc); break;
-      default: twin_body<N, 3>(tile, cp, xsb, lane, half, acc); break;
-    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[r][k] = words[kP / 4 + k] ^ 0x80808080u;
+    sa[r] = make_scale(scales & 0xFFFFu);
+    sb[r] = make_scale(scales >> 16);
   }
+  const uint8_t *xcol = xsb + (32 * B) * 4 + ch * 64;  // column 32b + 16ch of stream 0
+  uint64_t pa[kTaskSlots][N], pb[kTaskSlots][N];
+  static_for<0, 4>([&](auto jc) {  // two payload words (four columns) per step
+    constexpr int k0 = 2 * decltype(jc)::value;
+    ulonglong2 xa[N], xb[N];
+#pragma unroll
+    for (int s = 0; s < N; ++s) {
+      xa[s] = *reinterpret_cast<const ulonglong2 *>(xcol + s * kXS + k0 * 8);
+      xb[s] = *reinterpret_cast<const ulonglong2 *>(xcol + (N + s) * kXS + k0 * 8);
+    }
+    static_for<0, 2>([&](auto kk_) {
+      constexpr int kk = decltype(kk_)::value;
+      constexpr int k = k0 + kk;
+#pragma unroll
+      for (int r = 0; r < kTaskSlots; ++r) {
+        const uint64_t wa = dequant2(w[r][k], 1, w[r][k], 3, sa[r]);
+        const uint64_t wb = dequant2(w[r][k], 0, w[r][k], 2, sb[r]);
+#pragma unroll
+        for (int s = 0; s < N; ++s) {
+          const uint64_t x_a = kk ? xa[s].y : xa[s].x;
+          const uint64_t x_b = kk ? xb[s].y : xb[s].x;
+          if constexpr (k == 0) {
+            pa[r][s] = fmul2(wa, x_a);
+            pb[r][s] = fmul2(wb, x_b);
+          } else {
+            pa[r][s] = ffma2(wa, x_a, pa[r][s]);
+            pb[r][s] = ffma2(wb, x_b, pb[r][s]);
+          }
+        }
+      }
+    });
+  });
+#pragma unroll
+  for (int r = 0; r < kTaskSlots; ++r)
+#pragma unroll
+    for (int s = 0; s < N; ++s) {
+      acc[r][s] = fadd2(acc[r][s], pa[r][s]);
+      acc[r][N + s] = fadd2(acc[r][N + s], pb[r][s]);
+    }
 }
 
 __device__ __forceinline__ int32_t cta_of_unit(int64_t u, int64_t units, int32_t grid) {
@@ -514,7 +389,8 @@ __device__ __forceinline__ void down_epilogue(const GemvArgs &a, const float *ti
 }
 
 // Consumer warp q (0..7) of the warps that computed half h of a tile.  Q8:
-// warp w covers block w % 8 of half w / 8; twin: warp w covers half (w / 4) % 2.
+// warp w covers block w % 8 of half w / 8; twin: warp w covers columns
+// 16 (w / 8) .. 16 (w / 8) + 15 of block w % 4 in half (w / 4) % 2.
 template <Fmt F>
 __device__ __forceinline__ int red_warp(int q, int h) {
   if constexpr (F == Fmt::Q8) return 8 * h + q;
@@ -978,21 +854,23 @@ __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
       default: run(std::integral_constant<int, 1>{}, std::integral_constant<int, 1>{}); break;
     }
   } else {
-    // Twin: warp w runs on scheduler k = w % 4 and always works on the same two
-    // 16-byte chunks of every unit, rows of half j % 2 (j = w / 4): chunks
-    // k + 4(j/2) and k + 4(j/2) + 8, so each scheduler owns chunks k, k+4, k+8,
-    // k+12.  Chunk 16 of unit i goes to the warps j = 0, 1 of scheduler i % 4.
-    const uint32_t sched = warp & 3u, wj = warp >> 2;
-    const uint32_t half = wj & 1u;
-    const int ca = static_cast<int>(sched + 4u * (wj >> 1));
-    const ChunkParams pa = chunk_params<F, N>(ca), pb = chunk_params<F, N>(ca + 8), p16 = chunk_params<F, N>(16);
-    const bool takes16 = (wj >> 1) == 0u;
-    consumer_loop<F, N, E>(a, cx, [&](const uint8_t *tile, const uint8_t *xsb, int64_t i,
-                                      uint64_t (&acc)[kTaskSlots][kOut]) {
-      run_chunk<F, N>(pa, tile, xsb, lane, half, acc);
-      run_chunk<F, N>(pb, tile, xsb, lane, half, acc);
-      if (takes16 && (static_cast<uint32_t>(i) & 3u) == sched) run_chunk<F, N>(p16, tile, xsb, lane, half, acc);
-    }, release);
+    // Twin: warp w computes block b = w % 4 (its scheduler, so one code body
+    // per scheduler) of every unit, columns 16 ch .. 16 ch + 15 of the block
+    // (ch = w / 8), for the rows of half (w / 4) % 2.
+    const uint32_t half = (warp >> 2) & 1u, ch = warp >> 3;
+    auto run = [&](auto bc) {
+      constexpr int B_ = decltype(bc)::value;
+      consumer_loop<F, N, E>(a, cx, [&](const uint8_t *tile, const uint8_t *xsb, int64_t,
+                                        uint64_t (&acc)[kTaskSlots][kOut]) {
+        twin_block_body<N, B_>(tile, xsb, lane, half, ch, acc);
+      }, release);
+    };
+    switch (warp & 3u) {
+      case 0: run(std::integral_constant<int, 0>{}); break;
+      case 1: run(std::integral_constant<int, 1>{}); break;
+      case 2: run(std::integral_constant<int, 2>{}); break;
+      default: run(std::integral_constant<int, 3>{}); break;
+    }
   }
 }
 
