@@ -190,7 +190,9 @@ class Q8Pass:
         self.weight_bytes = rows * (cols // 32) * Q8_BLOCK
         self.launch_bytes = self.weight_bytes + 4 * n * (rows + cols)
         self.step_bytes = layers * self.launch_bytes
-        self.launches_per_step = layers
+        # each GEMV launch is followed by the launch that combines its shared tiles
+        self.launches_per_step = 2 * layers
+        self.gemv_launches_per_step = layers
         self.tokens_per_step = n
         self.dominant = "gemv_tma_kernel<Q8,%d>" % n
         self.dtype = "f32"
@@ -255,7 +257,8 @@ class TwinPass(Q8Pass):
         self.weight_bytes = rows * (cols // 32) * TWIN_BLOCK
         self.launch_bytes = self.weight_bytes + 4 * self.n * (rows + cols)
         self.step_bytes = layers * self.launch_bytes
-        self.launches_per_step = layers
+        self.launches_per_step = 2 * layers  # GEMV + tile combine
+        self.gemv_launches_per_step = layers
         self.tokens_per_step = self.n
         self.dominant = f"gemv_tma_kernel<Twin,{per_model}>"
         self.dtype = "f32"
@@ -418,7 +421,9 @@ class DecodePass(Q8Pass):
         act = 4 * n * ((hidden + ffn) + (ffn + hidden))
         self.step_bytes = layers * (self.weight_bytes + act) + 4 * n * 2 * hidden
         self.launch_bytes = self.step_bytes / (2 * layers)       # mean over the pass's GEMV launches
-        self.launches_per_step = 2 * layers + 1
+        # per layer: gate/up GEMV, its tile combine, down GEMV, its tile combine;
+        # then the final RMS kernel
+        self.launches_per_step = 4 * layers + 1
         self.gemv_launches_per_step = 2 * layers
         self.tokens_per_step = n
         self.dominant = f"gemv_tma_kernel<Q8,{n},GateUp|Down> (the pass's {2 * layers} GEMV launches)"
