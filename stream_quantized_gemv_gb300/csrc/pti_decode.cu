@@ -43,7 +43,7 @@ constexpr int kMaxLaunches = 64;         // so at most 4096 layers per call
 // Workspace of one pass, byte offsets (each 256-byte aligned).
 struct DecodeLayout {
   int64_t n_rb_gu = 0, n_rb_down = 0;  // tiles of the GateUp and Down kernels
-  size_t part = 0, tickets = 0, counter = 0, grid_bars = 0, h = 0, xraw = 0, sq_h = 0, sq_x = 0, total = 0;
+  size_t part = 0, tickets = 0, counter = 0, grid_bars = 0, h = 0, xraw = 0, sq_h = 0, sq_x = 0, scales = 0, total = 0;
 };
 
 size_t round256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
@@ -69,6 +69,8 @@ DecodeLayout decode_layout(int64_t hidden, int64_t ffn, int n) {
   off = round256(off + static_cast<size_t>(d.n_rb_gu) * n * sizeof(float));
   d.sq_x = off;
   off = round256(off + static_cast<size_t>(d.n_rb_down) * n * sizeof(float));
+  d.scales = off;  // the chained pass: input scales of the GateUp and of the Down step, [2][n]
+  off = round256(off + 2 * static_cast<size_t>(n) * sizeof(float));
   d.total = off;
   return d;
 }
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) rms_finalize_kernel(const Fi
       s2 += static_cast<double>(__ldcg(f.sq_x + static_cast<int64_t>(t) * N + warp));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xFFFFFFFFu, s2, o);
-    if (lane == 0) scale[warp] = static_cast<float>(1.0 / sqrt(s2 * f.inv_hidden + f.eps));
+    if (lane == 0) scale[warp] = rms_inv_scale(s2, f.inv_hidden, f.eps);
   }
   __syncthreads();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kFinalizeThreads;
@@ -299,7 +301,7 @@ __global__ void __launch_bounds__(kWarpCount * 32 + 32, 1)
         if (lane == 0) {
 #pragma unroll
           for (int s = 0; s < kOut; ++s)
-            scale[s] = ph.sq_in != nullptr ? static_cast<float>(1.0 / sqrt(s2[s] * ph.inv_len + P.eps)) : 1.0f;
+            scale[s] = ph.sq_in != nullptr ? rms_inv_scale(s2[s], ph.inv_len, P.eps) : 1.0f;
           mbar_arrive(scale_bar);
         }
       };
@@ -516,10 +518,12 @@ pti_status run_decode_chained(const void *const *w_gate, const void *const *w_up
   float *const xraw = reinterpret_cast<float *>(ws + d.xraw);
   float *const sq_h = reinterpret_cast<float *>(ws + d.sq_h);
   float *const sq_x = reinterpret_cast<float *>(ws + d.sq_x);
+  float *const scales = reinterpret_cast<float *>(ws + d.scales);
   GemvArgs base = {};
   base.part = reinterpret_cast<float *>(ws + d.part);
   base.tickets = reinterpret_cast<unsigned int *>(ws + d.tickets);
   base.eps = eps;
+  base.prefetch_all = 1;
   for (int l = 0; l < n_layers; ++l) {
     GemvArgs gu = base;
     gu.x0 = (l == 0) ? x_in : xraw;
@@ -530,6 +534,7 @@ pti_status run_decode_chained(const void *const *w_gate, const void *const *w_up
     gu.n_sq_in = static_cast<int32_t>(d.n_rb_down);
     gu.inv_len_in = 1.0 / static_cast<double>(hidden);
     gu.sq_out = sq_h;
+    gu.scale_out = scales;
     if (const pti_status s = launch_gemv<Fmt::Q8, N, Epi::GateUp>(w_gate[l], w_up[l], gu, stream, l > 0);
         s != PTI_OK)
       return s;
@@ -542,6 +547,7 @@ pti_status run_decode_chained(const void *const *w_gate, const void *const *w_up
     dn.n_sq_in = static_cast<int32_t>(d.n_rb_gu);
     dn.inv_len_in = 1.0 / static_cast<double>(ffn);
     dn.sq_out = sq_x;
+    dn.scale_out = scales + N;
     if (const pti_status s = launch_gemv<Fmt::Q8, N, Epi::Down>(w_down[l], nullptr, dn, stream, true); s != PTI_OK)
       return s;
   }

@@ -137,6 +137,10 @@ struct GemvArgs {
   double eps;          // added to the mean square before the square root
   int32_t n_sq_in;
   int32_t combine_in_kernel;  // 1: tickets and the last CTA combine shared tiles; 0: combine_tiles_kernel does
+  // Fused epilogues of the chained pass: the input scales the GEMV derived, for
+  // its tile-combine kernel ([kOut] floats, written by CTA 0).
+  float *scale_out;
+  int32_t prefetch_all;  // 1: fetch every initial stage's weights before waiting for the previous kernel
 };
 
 // Rows handled by one consumer warp: lane l owns rows 64h + l and 64h + 32 + l
@@ -310,30 +314,88 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// RMS scale of each input vector, 1 / sqrt(mean(v^2) + eps), from the
-// previous kernel's per-tile sums of squares (summed in double, in a fixed
-// order, so every CTA derives the same scale); 1 when there are none.
-// Warp s < kOut handles vector s; must run after the wait on the previous
-// kernel.  A consumer barrier must separate it from the first reader.
-template <int kOut>
-__device__ __forceinline__ void input_scales_body(const GemvArgs &a, uint32_t warp, uint32_t lane, float *scale) {
-  if (warp >= static_cast<uint32_t>(kOut)) return;
-  double s2 = 0.0;
-  if (a.sq_in != nullptr) {
-#pragma unroll 4
-    for (int32_t t = static_cast<int32_t>(lane); t < a.n_sq_in; t += 32)
-      s2 += static_cast<double>(__ldcg(a.sq_in + static_cast<int64_t>(t) * kOut + warp));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xFFFFFFFFu, s2, o);
-  if (lane == 0) scale[warp] = a.sq_in != nullptr ? static_cast<float>(1.0 / sqrt(s2 * a.inv_len_in + a.eps)) : 1.0f;
+// RMS scale 1 / sqrt(mean + eps) of a vector whose sum of squares is s2 (in
+// double), rounded to float.  A float reciprocal square root (relative error
+// below 2^-21) refined by one Newton step in double leaves a relative error
+// near 1e-13 before the final rounding, so the float result is the correctly
+// rounded scale except for values within that distance of a rounding
+// boundary (then it is one ulp away).  This replaces a double square root and
+// division: this GPU's double-precision unit is slow, and the scale sits on
+// the path from one decode step to the next.  A zero or non-finite argument
+// takes the plain formula.
+__device__ __forceinline__ float rms_inv_scale(double s2, double inv_len, double eps) {
+  const double m = s2 * inv_len + eps;
+  const float r0 = rsqrtf(static_cast<float>(m));
+  if (!(r0 > 0.0f) || !isfinite(r0) || !(m > 0.0)) return static_cast<float>(1.0 / sqrt(m));
+  const double r = static_cast<double>(r0);
+  return static_cast<float>(r * fma(-0.5 * m * r, r, 1.5));
 }
 
-// Out of line for the GEMV's consumers (one shared copy keeps their
-// instruction footprint small).
+// Staging of the fused epilogues' input sums: the per-tile sums of squares of
+// the previous kernel's output ([n_sq_in][kOut] floats) are bulk-copied into
+// a kSqStageBytes buffer of shared memory right after the wait on that
+// kernel.  The copy is rounded up to 16 bytes; the workspace pads every such
+// array to 256 bytes, so the few bytes past its end are still workspace.
+// Returns 0 when there is nothing to stage (no input sums, or more than the
+// buffer holds: then the sums are read from global memory).
+constexpr int kSqStageBytes = 4608;  // 288 tiles of 4 streams
+
 template <int kOut>
-__device__ __noinline__ void input_scales(const GemvArgs &a, uint32_t warp, uint32_t lane, float *scale) {
-  input_scales_body<kOut>(a, warp, lane, scale);
+__device__ __forceinline__ uint32_t staged_sum_bytes(const GemvArgs &a) {
+  if (a.sq_in == nullptr) return 0u;
+  const uint32_t bytes = (static_cast<uint32_t>(a.n_sq_in) * kOut * 4u + 15u) & ~15u;
+  return bytes <= static_cast<uint32_t>(kSqStageBytes) ? bytes : 0u;
+}
+
+// Float-float accumulator: the pair (hi, lo) holds the value hi + lo exactly
+// as long as no term is lost (Knuth's TwoSum makes each addition error-free;
+// the error terms are gathered in lo), which keeps the sum of a few hundred
+// positive floats to within a few 1e-15 relative (checked against exact
+// rational sums), on the single-precision pipe.
+struct F2Sum {
+  float hi, lo;
+};
+
+__device__ __forceinline__ F2Sum f2_add(F2Sum x, float h2, float l2) {
+  const float s = x.hi + h2;
+  const float bb = s - x.hi;
+  const float e = (x.hi - (s - bb)) + (h2 - bb);  // x.hi + h2 == s + e exactly
+  const float t = e + (x.lo + l2);
+  const float hi = s + t;
+  return F2Sum{hi, t - (hi - s)};
+}
+
+// RMS scale of input vector s, 1 / sqrt(mean(v^2) + eps), from the previous
+// kernel's per-tile sums of squares (staged in shared memory at `stage`, or
+// read from global memory when stage == 0), computed by one warp in a fixed
+// order, so every CTA derives the same scale; 1 when there are none.  Lane l
+// accumulates tiles l, l + 32, ... in a float-float sum, a fixed butterfly
+// combines the lanes, and the mean and scale are formed in double.  (This
+// GPU's double-precision pipe is slow, in latency and in throughput; the sum
+// runs on the single-precision pipe instead.)  Lane 0 writes scale[s].
+template <int kOut>
+__device__ __noinline__ void input_scale_of_stream(const GemvArgs &a, uint32_t stage, uint32_t s, uint32_t lane,
+                                                   float *scale) {
+  F2Sum acc{0.0f, 0.0f};
+  if (a.sq_in != nullptr) {
+    if (stage != 0u) {
+      for (int32_t t = static_cast<int32_t>(lane); t < a.n_sq_in; t += 32)
+        acc = f2_add(acc, __uint_as_float(lds32(stage + (static_cast<uint32_t>(t) * kOut + s) * 4u)), 0.0f);
+    } else {
+      for (int32_t t = static_cast<int32_t>(lane); t < a.n_sq_in; t += 32)
+        acc = f2_add(acc, __ldcg(a.sq_in + static_cast<int64_t>(t) * kOut + s), 0.0f);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float h2 = __shfl_xor_sync(0xFFFFFFFFu, acc.hi, o);
+    const float l2 = __shfl_xor_sync(0xFFFFFFFFu, acc.lo, o);
+    acc = f2_add(acc, h2, l2);
+  }
+  if (lane == 0) {
+    const double s2 = static_cast<double>(acc.hi) + static_cast<double>(acc.lo);
+    scale[s] = a.sq_in != nullptr ? rms_inv_scale(s2, a.inv_len_in, a.eps) : 1.0f;
+  }
 }
 
 // Decode-pass epilogue of gate/up tile rb: the tile's rows 0..63 are gate rows
@@ -544,8 +606,8 @@ __device__ __noinline__ void finish_tiles(const GemvArgs &a, const float *red, i
 // the fused epilogue on them.  Launched right after the GEMV with
 // programmatic dependent launch: it is resident early, works out which CTAs
 // share its tile (CTAs of unshared tiles exit at once) and only then waits
-// for the GEMV; after the wait every load it needs (the partials, the input's
-// sums of squares) is issued before the first is used.
+// for the GEMV; after the wait every load it needs (the partials, the input
+// scales the GEMV derived) is issued before the first is used.
 constexpr int kCombineThreads = 512;
 
 template <Fmt F, int N, Epi E>
@@ -553,7 +615,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_tiles_kernel(const __
   constexpr int kOut = Traits<F, N>::kOut;
   static_assert(kOut * kRowsPerTile <= kCombineThreads, "one element per thread");
   __shared__ float epi[kEpiBytes / 4];
-  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
+  const uint32_t tid = threadIdx.x;
   pdl_launch_dependents();
   const int32_t rb = static_cast<int32_t>(blockIdx.x);
   const int32_t c_lo = cta_of_unit(static_cast<int64_t>(rb) * a.n_sb, a.units, a.grid);
@@ -565,7 +627,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_tiles_kernel(const __
   pdl_wait_primary();
   float total = 0.0f;
   if (t < kOut * kRowsPerTile) total = sum_partials<kOut>(a, c_lo, c_hi, lo_slot, s, row);
-  if constexpr (E != Epi::Plain) input_scales_body<kOut>(a, warp, lane, epi + 4 * kRowsPerTile);
+  if constexpr (E != Epi::Plain)
+    if (tid < static_cast<uint32_t>(kOut)) epi[4 * kRowsPerTile + tid] = __ldcg(a.scale_out + tid);
   if (t < kOut * kRowsPerTile) deliver<F, N, E>(a, epi, rb, s, row, total);
   if constexpr (E != Epi::Plain) {
     named_barrier(kBarConsumers, kCombineThreads);
@@ -580,6 +643,8 @@ struct ConsumerCtx {
   float *epi;               // fused-epilogue scratch
   volatile uint32_t *flag;  // [0] abort, [1] last-arriver flag
   uint32_t bars, flags;     // shared addresses of the barriers and flags
+  uint32_t sq_bar;          // fused epilogues: completes when the input's per-tile sums are staged
+  uint32_t sq_stage;        // shared address of the staged sums
   int stages;
   uint32_t tid, warp, lane;
   int64_t u0, u1;           // this CTA's unit range
@@ -597,6 +662,28 @@ __device__ __forceinline__ void consumer_loop(const GemvArgs &a, const ConsumerC
   uint64_t acc[kTaskSlots][kOut];
   uint32_t st = 0, ph = 0;  // ring slot and phase parity of unit i
   int64_t i = 0;
+  // The fused epilogues need the input scales.  The producer stages the
+  // input's per-tile sums in shared memory right after its wait on the
+  // previous kernel; warp s < kOut derives scale s from them when the first
+  // tile is finished (a few shared loads; deriving them earlier, in the
+  // stream, measured slower: the deriving warps fall behind and hold ring
+  // slots).  The consumer barrier before finish_tiles publishes the scales;
+  // CTA 0 also hands them to the tile-combine kernel.
+  bool scales_ready = (E == Epi::Plain) || c.warp >= static_cast<uint32_t>(kOut);
+  auto wait_scales = [&]() {
+    if (scales_ready) return;
+    scales_ready = true;
+    const bool staged = staged_sum_bytes<kOut>(a) != 0u;
+    if (staged && !mbar_try_wait(c.sq_bar, 0) && !mbar_wait_bounded(c.sq_bar, 0, c.flags)) {
+      if (c.flag[0] == 0) atomicOr(&g_device_error, PTI_DEVERR_FULL_TIMEOUT);
+      c.flag[0] = 1;
+      return;
+    }
+    if (!staged && a.sq_in != nullptr) pdl_wait_primary();  // the sums come from the previous kernel
+    float *const scale = c.epi + 4 * kRowsPerTile;
+    input_scale_of_stream<kOut>(a, staged ? c.sq_stage : 0u, c.warp, c.lane, scale);
+    if (c.lane == 0 && blockIdx.x == 0 && a.scale_out != nullptr) a.scale_out[c.warp] = scale[c.warp];
+  };
   const int32_t rb_first = static_cast<int32_t>(c.u0 / a.n_sb);
   const int32_t rb_last = static_cast<int32_t>((c.u1 - 1) / a.n_sb);
   for (int32_t rb = rb_first; rb <= rb_last; ++rb) {
@@ -644,11 +731,13 @@ __device__ __forceinline__ void consumer_loop(const GemvArgs &a, const ConsumerC
     if (middle) {
       // a tile wholly inside this CTA's range: finish it now (rare: only when
       // a CTA spans more than two row tiles)
+      wait_scales();
       named_barrier(kBarConsumers, kConsumerThreads);
       finish_tiles<F, N, E>(a, c.red, 1, rb, 1, 0, 0, c.tid, c.flag, c.epi);
       named_barrier(kBarConsumers, kConsumerThreads);
     }
   }
+  wait_scales();
   named_barrier(kBarConsumers, kConsumerThreads);
   finish_tiles<F, N, E>(a, c.red, rb_last != rb_first ? 2 : 1, rb_first, 0, rb_last, 1, c.tid, c.flag, c.epi);
 }
@@ -669,6 +758,7 @@ struct Producer {
   int stages;
   int64_t u0, nu, issued;
   uint64_t pol;
+  uint32_t sq_bar, sq_stage;  // fused epilogues: barrier and buffer of the staged input sums
 
   __device__ __forceinline__ void coords(int64_t i, int32_t &rb, int32_t &sb) const {
     const int64_t u = u0 + i;
@@ -710,29 +800,39 @@ struct Producer {
   }
   // Weights do not depend on the previous kernel in the stream: fetch the
   // first tiles before waiting for it, then their activations.  When the
-  // consumers are the slower side (Q8 with N >= 2), only kRamp stages go out
-  // at once and each further initial stage waits until the one kRamp before
+  // consumers are the slower side (Q8 with N >= 2), only `ramp` stages go out
+  // at once and each further initial stage waits until the one `ramp` before
   // it has landed: with every SM requesting its whole ring at the same moment
   // the first stage would otherwise land only after most of the burst
-  // (measured: about 4 us), and compute could not start before.
+  // (measured: about 4 us), and compute could not start before.  Chained
+  // decode-pass launches (prefetch_all) fetch every initial stage before the
+  // wait: the previous kernel's tile combine leaves time for all of them.
   __device__ __forceinline__ void start() {
     prefetch_tmap(tmap);
     if constexpr (E == Epi::GateUp) prefetch_tmap(tmap2);
-    constexpr int64_t kRamp = (F == Fmt::Q8 && N >= 2) ? 2 : kMaxStages;
+    const int64_t ramp = (F == Fmt::Q8 && N >= 2 && !a->prefetch_all) ? 2 : kMaxStages;
     const int64_t pre = nu < stages ? nu : stages;
-    const int64_t first = pre < kRamp ? pre : kRamp;
+    const int64_t first = pre < ramp ? pre : ramp;
     for (int64_t i = 0; i < first; ++i) {
       mbar_expect_tx(bars + 8 * i, kStageBytes);
       load_w(i, static_cast<uint32_t>(i));
     }
     pdl_wait_primary();
+    if constexpr (E != Epi::Plain) {
+      // The input's per-tile sums of squares, for the consumers' scales.
+      const uint32_t bytes = staged_sum_bytes<T::kOut>(*a);
+      if (bytes != 0u) {
+        mbar_arrive_expect_tx(sq_bar, bytes);
+        bulk_load(sq_stage, a->sq_in, bytes, sq_bar);
+      }
+    }
     for (int64_t i = 0; i < first; ++i) {
       mbar_arrive_expect_tx(bars + 8 * i, S::kXBytes);
       load_x(i, static_cast<uint32_t>(i));
     }
     issued = first;
     for (int64_t i = first; i < pre; ++i) {
-      const uint32_t landed = bars + 8 * static_cast<uint32_t>(i - kRamp);
+      const uint32_t landed = bars + 8 * static_cast<uint32_t>(i - ramp);
       if (!mbar_try_wait(landed, 0) && !mbar_wait_bounded(landed, 0, flags)) {
         if (flag[0] == 0) atomicOr(&g_device_error, PTI_DEVERR_FULL_TIMEOUT);
         flag[0] = 1;
@@ -786,9 +886,11 @@ __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
   const int stages = a.stages;
   float *const red = reinterpret_cast<float *>(base_ptr + stages * S::kBytes);  // [2][warps][kOut][64]
   const uint32_t bars = base + stages * S::kBytes + S::kRedBytes;             // full[stages], empty[stages]
-  const uint32_t flags = bars + 2 * stages * 8;
+  const uint32_t flags = bars + 2 * stages * 8;  // flag words [0], [1]; then the barrier of the staged sums
+  const uint32_t sq_bar = flags + 8;
   volatile uint32_t *const flag = reinterpret_cast<volatile uint32_t *>(base_ptr + (flags - base));
   float *const epi = reinterpret_cast<float *>(base_ptr + (flags - base) + 16);  // kEpiBytes (fused epilogues)
+  const uint32_t sq_stage = flags + 16 + kEpiBytes;  // fused epilogues: kSqStageBytes of staged input sums
 
   const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t u0 = static_cast<int64_t>(blockIdx.x) * a.units / a.grid;
@@ -799,6 +901,7 @@ __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
       mbar_init(bars + 8 * i, 1);
       mbar_init(bars + 8 * (stages + i), kConsumerWarps);
     }
+    mbar_init(sq_bar, 1);
     flag[0] = 0;
     flag[1] = 0;
     mbar_init_fence();
@@ -810,7 +913,7 @@ __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
     // ---------------- producer: one lane issues every copy --------------------
     if (lane == 0) {
       Producer<F, N, E> prod{&tmap, &tmap2, &a, base, bars, flags, flag, stages, u0, u1 - u0, 0,
-                             l2_policy_evict_first()};
+                             l2_policy_evict_first(), sq_bar, sq_stage};
       prod.start();
       uint32_t st = 0, ph = 0;
       for (int64_t i = 0; i + stages < prod.nu && flag[0] == 0; ++i) {
@@ -826,11 +929,7 @@ __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
   }
 
   // ---------------- consumers ----------------------------------------------
-  if constexpr (E != Epi::Plain) {
-    pdl_wait_primary();  // the input's sums of squares come from the previous kernel
-    input_scales<kOut>(a, warp, lane, epi + 4 * kRowsPerTile);
-  }
-  const ConsumerCtx cx{base_ptr, red, epi, flag, bars, flags, stages, tid, warp, lane, u0, u1};
+  const ConsumerCtx cx{base_ptr, red, epi, flag, bars, flags, sq_bar, sq_stage, stages, tid, warp, lane, u0, u1};
   auto release = [](int64_t, uint32_t, uint32_t) {};
   if constexpr (F == Fmt::Q8) {
     // Warp w always computes block b = w % 8 of every unit for the rows of half
@@ -914,7 +1013,7 @@ TilePlan plan_tiles(int64_t rows, int64_t cols, int sms) {
   p.n_rb = (rows + out_rows_per_tile<E>() - 1) / out_rows_per_tile<E>();
   p.units = p.n_sb * p.n_rb;
   p.grid = static_cast<int32_t>(std::min<int64_t>({static_cast<int64_t>(sms), p.units, kMaxGrid}));
-  const int64_t fixed = 1024 + S::kRedBytes + 16 * kMaxStages + 16 + (E == Epi::Plain ? 0 : kEpiBytes);
+  const int64_t fixed = 1024 + S::kRedBytes + 16 * kMaxStages + 16 + (E == Epi::Plain ? 0 : kEpiBytes + kSqStageBytes);
   p.stages = static_cast<int32_t>(std::min<int64_t>(kMaxStages, (kSmemOptin - fixed) / S::kBytes));
   p.smem = static_cast<size_t>(fixed) + static_cast<size_t>(p.stages) * S::kBytes;
   return p;
