@@ -15,6 +15,9 @@
  *   pti_mlp_decode_pass   a chained decode pass: n_layers gated-MLP layers
  *                         (gate, up, SiLU, RMS, down, RMS) over 1..4 streams,
  *                         one pass over the weights for all streams.
+ *   pti_selfspec_greedy   greedy self-speculative decoding of a toy model on
+ *                         1..4 streams, device-resident (window update on the
+ *                         GPU, no host synchronisation per step).
  *
  * Sources are cited by page title and section:
  *   [PTI-forum]  "Packed Twin Inference：无需草稿模型的推测解码新方案，实现2倍吞吐量提升"
@@ -308,8 +311,10 @@ pti_status pti_verify_sample(const float *logits, const int32_t *guess, const fl
  * vectors is needed).  A last kernel applies the final RMS scale.  How the
  * steps are launched: see pti_mlp_decode_pass_ex.  The first launch waits for
  * all earlier work in the stream.
- * Arithmetic: GEMVs as in the conventions, SiLU with expf, RMS scales in
- * double from fp32 per-tile sums of squares; bit-reproducible run to run.
+ * Arithmetic: GEMVs as in the conventions, SiLU with expf, RMS scales from
+ * fp32 per-tile sums of squares summed exactly enough (float-float, about
+ * 1e-15 relative) and a float reciprocal square root refined in double;
+ * bit-reproducible run to run.
  */
 size_t pti_mlp_decode_pass_workspace_bytes(int64_t hidden, int64_t ffn, int n_streams);
 
@@ -340,6 +345,69 @@ pti_status pti_mlp_decode_pass_ex(const void *const *w_gate, const void *const *
                                   const float *x_in, float *x_out,
                                   void *workspace, size_t workspace_bytes,
                                   pti_stream_t stream, uint32_t flags);
+
+/*
+ * Greedy self-speculative decoding of a toy model, on the device.
+ *   [PTI-readme] §"接受机制如何工作": in each step stream 0 runs the model on
+ *   the last confirmed token (position n) and stream i >= 1 on a guess for
+ *   position n + i taken from the previous step; one weight pass serves all
+ *   streams ([PTI-forum] §"技术实现架构", steps 2-4: the streams' outputs are
+ *   compared, the confirmed text is extended by the accepted guesses, the
+ *   streams past the first rejection restart).  The pages give the loop only
+ *   in outline; this library reads it as a window of n_streams positions
+ *   updated in place (Jacobi iteration):
+ *     a[i]  = argmax (lowest index on ties) of the model's logits for token
+ *             win[i], i.e. the model's next token after win[i];
+ *     L     = the number of leading i < n_streams - 1 with win[i+1] == a[i]
+ *             (exactly pti_verify_greedy's accepted length, guess = win);
+ *     a[0 .. L] are appended to the confirmed text (each is the model's
+ *     greedy continuation of a confirmed token, so the text is exactly the
+ *     model's greedy rollout from first_token: no quality loss);
+ *     win'[0] = a[L]; win'[j] = a[L + j] while L + j < n_streams, else
+ *     a[n_streams - 1] (the streams past the rejection restart from the
+ *     newest outputs).
+ *   The initial window is first_token in every stream.
+ * The toy model has no state beyond the input token (its logits depend on
+ * that token only), so a stream's "KV state" is its window token:
+ *     x = embedding[token]; x = one decode layer (pti_mlp_decode_pass);
+ *     logits = W_head x  (pti_q8_gemv_nstream, vocab rows, hidden columns).
+ *
+ *   model      HOST struct, read during the call: embedding [vocab][hidden]
+ *              fp32 (16-byte aligned), the layer's w_gate, w_up ([ffn]
+ *              [hidden/32] Q8 blocks), w_down ([hidden][ffn/32]) and w_head
+ *              ([vocab][hidden/32]), all DEVICE pointers, 16-byte aligned;
+ *              vocab 2 .. 2^24, hidden and ffn as pti_mlp_decode_pass,
+ *              eps finite >= 0.
+ *   n_streams  1..4 (1: plain greedy decoding, one token per step).
+ *   first_token  in [0, vocab).
+ *   steps      >= 0 decode steps, each one pass over the weights for all
+ *              streams; enqueued as 6 launches per step, no host
+ *              synchronisation.
+ *   tokens_out DEVICE [tokens_capacity] int32: the confirmed tokens after
+ *              first_token, in order; tokens past the capacity are counted
+ *              but not stored.
+ *   count_out  DEVICE int32: the number of confirmed tokens (sum over steps
+ *              of 1 + accept_out[step]).
+ *   accept_out DEVICE [steps] int32 (may be NULL): L of each step.
+ *   workspace  at least pti_selfspec_greedy_workspace_bytes(vocab, hidden,
+ *              ffn, n_streams) bytes, 256-byte aligned, scratch.
+ * Errors: invalid arguments return a status and enqueue nothing; the embedding
+ * and the tokens are checked only on the host side (pointers, alignment);
+ * a token is used as an index only after clamping to [0, vocab).
+ */
+typedef struct pti_toy_model {
+    const float *embedding;
+    const void *w_gate, *w_up, *w_down, *w_head;
+    int64_t vocab, hidden, ffn;
+    double eps;
+} pti_toy_model;
+
+size_t pti_selfspec_greedy_workspace_bytes(int64_t vocab, int64_t hidden, int64_t ffn, int n_streams);
+
+pti_status pti_selfspec_greedy(const pti_toy_model *model, int n_streams, int32_t first_token, int steps,
+                               int32_t *tokens_out, int64_t tokens_capacity, int32_t *count_out,
+                               int32_t *accept_out, void *workspace, size_t workspace_bytes,
+                               pti_stream_t stream);
 
 /*
  * Reads and clears the device error word of the current device (a blocking

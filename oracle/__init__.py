@@ -80,6 +80,9 @@ def _load():
             lib.pti_or_verify_sample.argtypes = [P, P, P, I64, I, I64, ctypes.c_double, P, P, P, P, P]
             lib.pti_or_mlp_layer.restype = I
             lib.pti_or_mlp_layer.argtypes = [P, P, P, I64, I64, I, ctypes.c_double, P, P, P]
+            lib.pti_or_selfspec_greedy.restype = I
+            lib.pti_or_selfspec_greedy.argtypes = [P, I64, I, ctypes.c_int32, I64, P, I64,
+                                                   ctypes.POINTER(ctypes.c_int64), P]
             _lib = lib
     return _lib
 
@@ -239,3 +242,47 @@ def mlp_layer(wg, wu, wd, hidden: int, ffn: int, x: np.ndarray, eps: float = 1e-
     _check(_load().pti_or_mlp_layer(_ptr(wg), _ptr(wu), _ptr(wd), hidden, ffn, n, eps,
                                     _ptr(x), _ptr(x_out), _ptr(h)), "mlp_layer")
     return x_out, h
+
+
+def selfspec_greedy(next_token: np.ndarray, n: int, first: int, steps: int):
+    """Greedy self-speculative decoding over the greedy next-token table
+    ``next_token`` [vocab] (pti_oracle.c, pti_or_selfspec_greedy).
+
+    Returns ``(tokens, accept)``: the confirmed tokens after ``first``
+    (int32 [count]) and the accepted length of every step (int32 [steps]).
+    """
+    nxt = np.ascontiguousarray(next_token, dtype=np.int32)
+    cap = steps * n
+    tokens = np.zeros(max(cap, 1), dtype=np.int32)
+    accept = np.zeros(max(steps, 1), dtype=np.int32)
+    count = ctypes.c_int64(0)
+    _check(_load().pti_or_selfspec_greedy(_ptr(nxt), nxt.size, n, first, steps, _ptr(tokens), cap,
+                                          ctypes.byref(count), _ptr(accept)), "selfspec_greedy")
+    return tokens[:count.value].copy(), accept[:steps].copy()
+
+
+def toy_logits(embedding, wg, wu, wd, wh, vocab: int, hidden: int, ffn: int, tokens, eps: float = 1e-6):
+    """fp64 logits [len(tokens)][vocab] of the toy model of the self-speculative
+    loop: x = embedding[token] (an fp32 table [vocab][hidden]), one decode
+    layer (``mlp_layer``), logits = W_head x (``q8_gemv``, vocab rows)."""
+    emb = np.asarray(embedding, dtype=np.float32).reshape(vocab, hidden)
+    x = emb[np.asarray(tokens, dtype=np.int64)]
+    xo, _ = mlp_layer(wg, wu, wd, hidden, ffn, x, eps)
+    # the C GEMV takes fp32 activations: split the fp64 layer output into an
+    # fp32 head and tail (x = hi + lo to about 2^-48 relative) and add the two
+    # fp64 products
+    hi = xo.astype(np.float32)
+    lo = (xo - hi.astype(np.float64)).astype(np.float32)
+    y, _ = q8_gemv(wh, vocab, hidden, np.concatenate([hi, lo]))
+    return y[:x.shape[0]] + y[x.shape[0]:]
+
+
+def greedy_next_table(logits: np.ndarray):
+    """The greedy next token (argmax, lowest index on ties) of each row of
+    ``logits`` [vocab][vocab] and its margin over the runner-up."""
+    lg = np.asarray(logits, dtype=np.float64)
+    nxt = np.argmax(lg, axis=1).astype(np.int32)
+    top = lg[np.arange(lg.shape[0]), nxt]
+    rest = lg.copy()
+    rest[np.arange(lg.shape[0]), nxt] = -np.inf
+    return nxt, top - rest.max(axis=1)

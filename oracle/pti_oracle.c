@@ -422,3 +422,48 @@ int pti_or_mlp_layer(const uint8_t *wg, const uint8_t *wu, const uint8_t *wd,
     free(h);
     return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * Greedy self-speculative decoding, [PTI-readme] §"接受机制如何工作" with the
+ * state handling of [PTI-forum] §"技术实现架构" (see pti_oracle.h for the
+ * reading).  The model is given by its greedy next-token table; one step is
+ * one pass of every stream through the model.
+ * ------------------------------------------------------------------------- */
+int pti_or_selfspec_greedy(const int32_t *next, int64_t vocab, int n, int32_t first, int64_t steps,
+                           int32_t *tokens, int64_t cap, int64_t *count, int32_t *accept)
+{
+    int32_t win[4], a[4];
+    int64_t t, v, c = 0;
+    int i, L;
+    if (next == NULL || count == NULL || n < 1 || n > 4 || vocab < 1 || steps < 0 || cap < 0)
+        return -1;
+    if ((cap > 0 && tokens == NULL) || first < 0 || first >= vocab)
+        return -1;
+    for (v = 0; v < vocab; ++v)
+        if (next[v] < 0 || next[v] >= vocab)
+            return -1;
+    for (i = 0; i < n; ++i)
+        win[i] = first;
+    for (t = 0; t < steps; ++t) {
+        /* every stream runs the model on its window token */
+        for (i = 0; i < n; ++i)
+            a[i] = next[win[i]];
+        /* stream i+1's input was a guess of what stream i produces */
+        L = 0;
+        while (L < n - 1 && win[L + 1] == a[L])
+            ++L;
+        /* a[0 .. L] are confirmed */
+        for (i = 0; i <= L; ++i) {
+            if (c < cap)
+                tokens[c] = a[i];
+            ++c;
+        }
+        if (accept != NULL)
+            accept[t] = L;
+        /* the next window starts at the newest confirmed token */
+        for (i = 0; i < n; ++i)
+            win[i] = a[(L + i < n) ? (L + i) : (n - 1)];
+    }
+    *count = c;
+    return 0;
+}

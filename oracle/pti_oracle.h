@@ -122,6 +122,24 @@ int pti_or_mlp_layer(const uint8_t *wg, const uint8_t *wu, const uint8_t *wd,
                      int64_t hidden, int64_t ffn, int n, double eps,
                      const double *x_in, double *x_out, double *h_out);
 
+/* Greedy self-speculative decoding of a model whose next token depends on the
+ * input token only ([PTI-readme] §"接受机制如何工作": stream 0 runs the model
+ * on the last confirmed token, stream i on a guess for position n + i taken
+ * from the previous step; [PTI-forum] §"技术实现架构", steps 2-4: compare the
+ * streams' outputs, extend the confirmed text with the accepted guesses,
+ * restart the rejected streams), read as a window updated in place:
+ *   a[i] = next[win[i]]                    (the greedy output of stream i)
+ *   L    = number of leading i < n-1 with win[i+1] == a[i]
+ *   confirmed text += a[0], ..., a[L]
+ *   win[0] = a[L]; win[j] = a[L+j] if L+j < n, else a[n-1]
+ * starting from win[i] = first for every stream.
+ *   next [vocab]     the model's greedy next token of each token
+ *   tokens [cap]     confirmed tokens after `first` (those past cap are counted,
+ *                    not stored); count: their number; accept [steps]: L
+ * Returns 0, or -1 on a bad argument (n in 1..4, next[] in [0, vocab)). */
+int pti_or_selfspec_greedy(const int32_t *next, int64_t vocab, int n, int32_t first, int64_t steps,
+                           int32_t *tokens, int64_t cap, int64_t *count, int32_t *accept);
+
 #ifdef __cplusplus
 }
 #endif

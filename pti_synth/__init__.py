@@ -165,6 +165,21 @@ def twin_matrix(rows: int, cols: int, seed: int, tensor_id: int = 0, identical: 
     return out.reshape(-1)
 
 
+def toy_model(vocab: int, hidden: int, ffn: int, seed: int) -> dict:
+    """Synthetic weights of the toy model of the self-speculative loop: an fp32
+    embedding table [vocab][hidden] N(0, 1), one gated-MLP layer (gate and up
+    [ffn][hidden], down [hidden][ffn], Q8) and an LM head [vocab][hidden] Q8,
+    each from its own tensor id."""
+    return {
+        "embedding": normal_f32(seed, 40, vocab * hidden).reshape(vocab, hidden),
+        "w_gate": q8_matrix(ffn, hidden, seed, tensor_id=41),
+        "w_up": q8_matrix(ffn, hidden, seed, tensor_id=42),
+        "w_down": q8_matrix(hidden, ffn, seed, tensor_id=43),
+        "w_head": q8_matrix(vocab, hidden, seed, tensor_id=44),
+        "vocab": vocab, "hidden": hidden, "ffn": ffn,
+    }
+
+
 def activations(n: int, cols: int, seed: int, tensor_id: int = 0) -> np.ndarray:
     """[n][cols] float32 N(0, 1), stream-major."""
     return normal_f32(seed, tensor_id, n * cols).reshape(n, cols)

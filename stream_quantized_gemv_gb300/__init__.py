@@ -94,6 +94,10 @@ def lib() -> ctypes.CDLL:
             L.pti_mlp_decode_pass_ex.restype = I
             L.pti_mlp_decode_pass_ex.argtypes = [P, P, P, I, I64, I64, I, ctypes.c_double, P, P, P, SZ, P,
                                                  ctypes.c_uint32]
+            L.pti_selfspec_greedy_workspace_bytes.restype = SZ
+            L.pti_selfspec_greedy_workspace_bytes.argtypes = [I64, I64, I64, I]
+            L.pti_selfspec_greedy.restype = I
+            L.pti_selfspec_greedy.argtypes = [ctypes.POINTER(ToyModel), I, ctypes.c_int32, I, P, I64, P, P, P, SZ, P]
             L.pti_device_error.restype = I
             L.pti_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             _lib = L
@@ -304,6 +308,42 @@ def mlp_decode_pass(weights, hidden: int, ffn: int, x, eps: float = 1e-6, x_out=
                                         0 if ws is None else ws.numel() * ws.element_size(), _stream(stream),
                                         FLAG_DECODE_PERSISTENT if persistent else 0), "pti_mlp_decode_pass")
     return x_out
+
+
+class ToyModel(ctypes.Structure):
+    """The C struct pti_toy_model (device pointers and sizes)."""
+    _fields_ = [("embedding", ctypes.c_void_p), ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p),
+                ("w_down", ctypes.c_void_p), ("w_head", ctypes.c_void_p), ("vocab", ctypes.c_int64),
+                ("hidden", ctypes.c_int64), ("ffn", ctypes.c_int64), ("eps", ctypes.c_double)]
+
+
+def selfspec_greedy_workspace_bytes(vocab: int, hidden: int, ffn: int, n_streams: int) -> int:
+    return lib().pti_selfspec_greedy_workspace_bytes(vocab, hidden, ffn, n_streams)
+
+
+def selfspec_greedy(embedding, w_gate, w_up, w_down, w_head, vocab: int, hidden: int, ffn: int, n_streams: int,
+                    first_token: int, steps: int, eps: float = 1e-6, capacity=None, ws=None, stream=None):
+    """Greedy self-speculative decoding of the toy model on ``n_streams``
+    streams for ``steps`` steps, resident on the device.  Returns
+    ``(tokens, count, accept)``: the confirmed-token buffer [capacity] int32
+    (default steps * n_streams), the device count [1] and the accepted
+    length of every step [steps], all device tensors."""
+    import torch
+    dev = embedding.device
+    cap = steps * n_streams if capacity is None else capacity
+    tokens = torch.zeros(max(cap, 1), dtype=torch.int32, device=dev)
+    count = torch.zeros(1, dtype=torch.int32, device=dev)
+    accept = torch.zeros(max(steps, 1), dtype=torch.int32, device=dev)
+    need = selfspec_greedy_workspace_bytes(vocab, hidden, ffn, n_streams)
+    if ws is None:
+        ws = workspace(need, dev)
+    model = ToyModel(embedding.data_ptr(), w_gate.data_ptr(), w_up.data_ptr(), w_down.data_ptr(),
+                     w_head.data_ptr(), vocab, hidden, ffn, float(eps))
+    _check(lib().pti_selfspec_greedy(ctypes.byref(model), n_streams, int(first_token), steps, _ptr(tokens), cap,
+                                     _ptr(count), _ptr(accept), _ptr(ws),
+                                     0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+           "pti_selfspec_greedy")
+    return tokens[:cap], count, accept[:steps]
 
 
 def device_error() -> int:

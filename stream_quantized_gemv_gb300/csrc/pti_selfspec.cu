@@ -1,0 +1,216 @@
+// pti_selfspec.cu -- device-resident greedy self-speculative decoding of a toy
+// model: the loop of [PTI-readme] "打包双子推理（PTI）" §"接受机制如何工作" and
+// [PTI-forum] "Packed Twin Inference：无需草稿模型的推测解码新方案，实现2倍吞吐量提升"
+// §"技术实现架构" (one weight pass for every stream, compare the streams'
+// outputs, extend the confirmed text with the accepted guesses, restart the
+// rejected streams), read as a window of positions updated in place.
+//
+// One step is six launches in one CUDA stream: the embedding gather, the
+// decode layer (two GEMVs with their tile combines and the final RMS kernel,
+// pti_mlp_decode_pass), the LM-head GEMV (pti_q8_gemv_nstream), greedy verify
+// (pti_verify_greedy) and the window update below.  The window and the
+// confirmed text stay in device memory, so steps are enqueued back to back
+// without a host round trip.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "pti.h"
+#include "pti_host.h"
+
+namespace pti {
+namespace {
+
+constexpr int kGatherThreads = 256;
+
+// x[s][:] = embedding[win[s]][:] for the n streams (the token clamped to
+// [0, vocab), so a corrupt window cannot index outside the table).
+__global__ void __launch_bounds__(kGatherThreads) embed_gather_kernel(const float *__restrict__ emb,
+                                                                      const int32_t *__restrict__ win, int n,
+                                                                      int64_t vocab, int64_t hidden,
+                                                                      float *__restrict__ x) {
+  const int s = static_cast<int>(blockIdx.y);
+  if (s >= n) return;
+  int64_t t = win[s];
+  t = t < 0 ? 0 : (t >= vocab ? vocab - 1 : t);
+  const float4 *src = reinterpret_cast<const float4 *>(emb + t * hidden);
+  float4 *dst = reinterpret_cast<float4 *>(x + static_cast<int64_t>(s) * hidden);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kGatherThreads + threadIdx.x; i < hidden / 4;
+       i += static_cast<int64_t>(gridDim.x) * kGatherThreads)
+    dst[i] = src[i];
+}
+
+// The window update after verify: the accepted length L and the argmax a[]
+// of the step give the confirmed tokens a[0 .. L] and the next window
+// win[0] = a[L], win[j] = a[L + j] (or a[n - 1] past the end).
+struct UpdateArgs {
+  int32_t *win;              // [n] the window (stream inputs)
+  const int32_t *argmax;     // [n]
+  const int32_t *accept;     // [1]
+  int32_t *tokens;           // [capacity] confirmed text
+  int64_t capacity;
+  int32_t *count;            // [1] confirmed tokens so far
+  int32_t *accept_log;       // [steps] or null
+  int step, n;
+};
+
+__global__ void __launch_bounds__(32) window_update_kernel(const UpdateArgs u) {
+  if (threadIdx.x != 0) return;
+  int32_t a[4];
+  for (int i = 0; i < u.n; ++i) a[i] = u.argmax[i];
+  int L = u.accept[0];
+  L = L < 0 ? 0 : (L > u.n - 1 ? u.n - 1 : L);
+  const int32_t c = u.count[0];
+  for (int i = 0; i <= L; ++i)
+    if (static_cast<int64_t>(c) + i < u.capacity) u.tokens[c + i] = a[i];
+  u.count[0] = c + L + 1;
+  if (u.accept_log != nullptr) u.accept_log[u.step] = L;
+  for (int j = 0; j < u.n; ++j) u.win[j] = a[(L + j < u.n) ? (L + j) : (u.n - 1)];
+}
+
+__global__ void __launch_bounds__(32) window_init_kernel(int32_t *win, int n, int32_t first, int32_t *count) {
+  if (threadIdx.x < static_cast<unsigned>(n)) win[threadIdx.x] = first;
+  if (threadIdx.x == 0) count[0] = 0;
+}
+
+size_t round256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+// Workspace: window, argmax, match, accept, x, y, logits, then the decode
+// pass's and the LM-head GEMV's own workspaces.
+struct SelfspecLayout {
+  size_t win = 0, argmax = 0, match = 0, accept = 0, x = 0, y = 0, logits = 0, decode = 0, gemv = 0, total = 0;
+  size_t decode_bytes = 0, gemv_bytes = 0;
+};
+
+SelfspecLayout selfspec_layout(int64_t vocab, int64_t hidden, int64_t ffn, int n) {
+  SelfspecLayout d;
+  size_t off = 0;
+  d.win = off;
+  off = round256(off + 4 * sizeof(int32_t));
+  d.argmax = off;
+  off = round256(off + 4 * sizeof(int32_t));
+  d.match = off;
+  off = round256(off + 4);
+  d.accept = off;
+  off = round256(off + sizeof(int32_t));
+  d.x = off;
+  off = round256(off + static_cast<size_t>(n) * hidden * sizeof(float));
+  d.y = off;
+  off = round256(off + static_cast<size_t>(n) * hidden * sizeof(float));
+  d.logits = off;
+  off = round256(off + static_cast<size_t>(n) * vocab * sizeof(float));
+  d.decode_bytes = pti_mlp_decode_pass_workspace_bytes(hidden, ffn, n);
+  d.decode = off;
+  off = round256(off + d.decode_bytes);
+  d.gemv_bytes = pti_q8_gemv_workspace_bytes(vocab, hidden, n);
+  d.gemv = off;
+  off = round256(off + d.gemv_bytes);
+  d.total = off;
+  return d;
+}
+
+// vocab in [2, 2^24]; hidden and ffn as the decode pass requires (then the
+// LM head, vocab rows by hidden columns, takes the GEMV's fast path).
+bool valid_model(const pti_toy_model *m) {
+  return m->vocab >= 2 && m->vocab <= (int64_t{1} << 24) &&
+         pti_mlp_decode_pass_workspace_bytes(m->hidden, m->ffn, 1) != 0;
+}
+
+}  // namespace
+}  // namespace pti
+
+using namespace pti;
+
+extern "C" size_t pti_selfspec_greedy_workspace_bytes(int64_t vocab, int64_t hidden, int64_t ffn, int n_streams) {
+  if (n_streams < 1 || n_streams > 4 || vocab < 2 || vocab > (int64_t{1} << 24)) return 0;
+  if (pti_mlp_decode_pass_workspace_bytes(hidden, ffn, n_streams) == 0) return 0;
+  return selfspec_layout(vocab, hidden, ffn, n_streams).total;
+}
+
+extern "C" pti_status pti_selfspec_greedy(const pti_toy_model *model, int n_streams, int32_t first_token,
+                                          int steps, int32_t *tokens_out, int64_t tokens_capacity,
+                                          int32_t *count_out, int32_t *accept_out, void *workspace,
+                                          size_t workspace_bytes, pti_stream_t stream) {
+  if (model == nullptr || count_out == nullptr || workspace == nullptr) return PTI_ERR_NULL;
+  if (model->embedding == nullptr || model->w_gate == nullptr || model->w_up == nullptr ||
+      model->w_down == nullptr || model->w_head == nullptr)
+    return PTI_ERR_NULL;
+  if (n_streams < 1 || n_streams > 4) return PTI_ERR_NSTREAMS;
+  if (steps < 0 || tokens_capacity < 0 || !valid_model(model)) return PTI_ERR_SHAPE;
+  if (tokens_capacity > 0 && tokens_out == nullptr) return PTI_ERR_NULL;
+  if (first_token < 0 || first_token >= model->vocab) return PTI_ERR_VALUE;
+  if (!std::isfinite(model->eps) || model->eps < 0.0) return PTI_ERR_VALUE;
+  if (!aligned(model->embedding, 16) || !aligned(model->w_gate, 16) || !aligned(model->w_up, 16) ||
+      !aligned(model->w_down, 16) || !aligned(model->w_head, 16) || !aligned(workspace, 256) ||
+      !aligned(count_out, 4) || (tokens_out != nullptr && !aligned(tokens_out, 4)) ||
+      (accept_out != nullptr && !aligned(accept_out, 4)))
+    return PTI_ERR_ALIGN;
+  const size_t need = pti_selfspec_greedy_workspace_bytes(model->vocab, model->hidden, model->ffn, n_streams);
+  if (need == 0) return PTI_ERR_SHAPE;
+  if (workspace_bytes < need) return PTI_ERR_WORKSPACE;
+  // Nothing written (the workspace, the outputs) may overlap anything read
+  // (the embedding, the weights): checked here, so that no launch of the
+  // loop can fail validation once the first has been enqueued.
+  const uint64_t emb_bytes = static_cast<uint64_t>(model->vocab) * model->hidden * 4;
+  const uint64_t gu_bytes = static_cast<uint64_t>(model->ffn) * (model->hidden / 32) * 34;
+  const uint64_t dn_bytes = static_cast<uint64_t>(model->hidden) * (model->ffn / 32) * 34;
+  const uint64_t hd_bytes = static_cast<uint64_t>(model->vocab) * (model->hidden / 32) * 34;
+  const void *const outs[4] = {workspace, tokens_out, count_out, accept_out};
+  const uint64_t out_bytes[4] = {workspace_bytes, static_cast<uint64_t>(tokens_capacity) * 4, 4,
+                                 static_cast<uint64_t>(steps) * 4};
+  for (int k = 0; k < 4; ++k)
+    if (overlaps(outs[k], out_bytes[k], model->embedding, emb_bytes) ||
+        overlaps(outs[k], out_bytes[k], model->w_gate, gu_bytes) ||
+        overlaps(outs[k], out_bytes[k], model->w_up, gu_bytes) ||
+        overlaps(outs[k], out_bytes[k], model->w_down, dn_bytes) ||
+        overlaps(outs[k], out_bytes[k], model->w_head, hd_bytes))
+      return PTI_ERR_ALIAS;
+  if (overlaps(workspace, workspace_bytes, tokens_out, static_cast<uint64_t>(tokens_capacity) * 4) ||
+      overlaps(workspace, workspace_bytes, count_out, 4) ||
+      overlaps(workspace, workspace_bytes, accept_out, static_cast<uint64_t>(steps) * 4) ||
+      overlaps(tokens_out, static_cast<uint64_t>(tokens_capacity) * 4, count_out, 4) ||
+      overlaps(accept_out, static_cast<uint64_t>(steps) * 4, count_out, 4) ||
+      overlaps(accept_out, static_cast<uint64_t>(steps) * 4, tokens_out, static_cast<uint64_t>(tokens_capacity) * 4))
+    return PTI_ERR_ALIAS;
+
+  const SelfspecLayout d = selfspec_layout(model->vocab, model->hidden, model->ffn, n_streams);
+  uint8_t *const ws = static_cast<uint8_t *>(workspace);
+  int32_t *const win = reinterpret_cast<int32_t *>(ws + d.win);
+  int32_t *const argmax = reinterpret_cast<int32_t *>(ws + d.argmax);
+  uint8_t *const match = ws + d.match;
+  int32_t *const accept = reinterpret_cast<int32_t *>(ws + d.accept);
+  float *const x = reinterpret_cast<float *>(ws + d.x);
+  float *const y = reinterpret_cast<float *>(ws + d.y);
+  float *const logits = reinterpret_cast<float *>(ws + d.logits);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  window_init_kernel<<<1, 32, 0, st>>>(win, n_streams, first_token, count_out);
+  if (cudaGetLastError() != cudaSuccess) return PTI_ERR_CUDA;
+  const int64_t chunks = model->hidden / 4;
+  const unsigned gx = static_cast<unsigned>((chunks + kGatherThreads - 1) / kGatherThreads);
+  const void *const wg[1] = {model->w_gate};
+  const void *const wu[1] = {model->w_up};
+  const void *const wd[1] = {model->w_down};
+  for (int step = 0; step < steps; ++step) {
+    embed_gather_kernel<<<dim3(gx, static_cast<unsigned>(n_streams)), kGatherThreads, 0, st>>>(
+        model->embedding, win, n_streams, model->vocab, model->hidden, x);
+    if (cudaGetLastError() != cudaSuccess) return PTI_ERR_CUDA;
+    if (const pti_status s = pti_mlp_decode_pass(wg, wu, wd, 1, model->hidden, model->ffn, n_streams, model->eps,
+                                                 x, y, ws + d.decode, d.decode_bytes, stream);
+        s != PTI_OK)
+      return s;
+    if (const pti_status s = pti_q8_gemv_nstream(model->w_head, model->vocab, model->hidden, n_streams, y, logits,
+                                                 ws + d.gemv, d.gemv_bytes, stream);
+        s != PTI_OK)
+      return s;
+    if (const pti_status s = pti_verify_greedy(logits, win, 1, n_streams, model->vocab, argmax,
+                                               n_streams > 1 ? match : nullptr, accept, stream);
+        s != PTI_OK)
+      return s;
+    UpdateArgs u{win, argmax, accept, tokens_out, tokens_capacity, count_out, accept_out, step, n_streams};
+    window_update_kernel<<<1, 32, 0, st>>>(u);
+    if (cudaGetLastError() != cudaSuccess) return PTI_ERR_CUDA;
+  }
+  return PTI_OK;
+}

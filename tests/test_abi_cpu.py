@@ -207,3 +207,37 @@ def test_twin_nstream_validation(L):
     assert L.pti_ssq_twin_gemv_nstream(*args, 2, xa, xb, ya, yb, None, 0, None, 0) == 7
     assert L.pti_ssq_twin_gemv_nstream_workspace_bytes(128, 512, 2) > L.pti_ssq_twin_gemv_nstream_workspace_bytes(128, 512, 1)
     assert L.pti_ssq_twin_gemv_nstream_workspace_bytes(128, 512, 3) == 0
+
+
+def _toy(emb=FAKE, gate=FAKE + (1 << 30), up=FAKE + (2 << 30), down=FAKE + (3 << 30), head=FAKE + (4 << 30),
+         vocab=512, hidden=256, ffn=256, eps=1e-6):
+    return pti.ToyModel(emb, gate, up, down, head, vocab, hidden, ffn, eps)
+
+
+def test_selfspec_validation(L):
+    """The self-speculative loop validates everything before its first launch."""
+    need = L.pti_selfspec_greedy_workspace_bytes(512, 256, 256, 4)
+    assert need > 0 and need % 256 == 0
+    assert L.pti_selfspec_greedy_workspace_bytes(1, 256, 256, 4) == 0
+    assert L.pti_selfspec_greedy_workspace_bytes(512, 100, 256, 4) == 0
+    assert L.pti_selfspec_greedy_workspace_bytes(512, 256, 256, 5) == 0
+    out, cnt, acc, ws = FAKE + (8 << 34), FAKE + (9 << 34), FAKE + (10 << 34), FAKE + (11 << 34)
+
+    def call(model=None, n=4, first=3, steps=8, tokens=out, cap=32, count=cnt, accept=acc, w=ws, wb=need):
+        m = _toy() if model is None else model
+        return L.pti_selfspec_greedy(ctypes.byref(m), n, first, steps, tokens, cap, count, accept, w, wb, None)
+
+    assert L.pti_selfspec_greedy(None, 4, 3, 8, out, 32, cnt, acc, ws, need, None) == 1
+    assert call(model=_toy(emb=None)) == 1 and call(model=_toy(head=None)) == 1
+    assert call(count=None) == 1 and call(w=None) == 1 and call(tokens=None) == 1
+    assert call(n=0) == 3 and call(n=5) == 3
+    assert call(steps=-1) == 2 and call(cap=-1) == 2
+    assert call(model=_toy(vocab=1)) == 2 and call(model=_toy(hidden=100)) == 2
+    assert call(first=-1) == 8 and call(first=512) == 8
+    assert call(model=_toy(eps=-1.0)) == 8 and call(model=_toy(eps=float("nan"))) == 8
+    assert call(model=_toy(emb=FAKE + 4)) == 4 and call(model=_toy(down=FAKE + (3 << 30) + 8)) == 4
+    assert call(w=ws + 16) == 4 and call(count=cnt + 2) == 4
+    assert call(wb=need - 1) == 7
+    assert call(w=FAKE + (4 << 30)) == 5                  # workspace over the LM head
+    assert call(tokens=FAKE + 64) == 5                     # tokens inside the embedding table
+    assert call(count=out + 8) == 5                        # count inside the token buffer

@@ -1,0 +1,90 @@
+"""GPU parity of the device-resident greedy self-speculative loop
+(pti_selfspec_greedy) with the oracle's loop (pti_or_selfspec_greedy) on the
+synthetic toy model: the confirmed tokens, their count and every step's
+accepted length must be identical.
+
+The oracle's greedy next-token table comes from fp64 logits; the test first
+checks that every token the loop can feed the model (the forward orbit of the
+first token under the table) has an argmax margin above the GPU's error bound,
+so the comparison is exact, not statistical.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pti_synth
+import stream_quantized_gemv_gb300 as pti
+
+pytestmark = pytest.mark.gpu
+
+V, H, F = 512, 256, 256
+
+
+@pytest.fixture(scope="module")
+def toy():
+    m = pti_synth.toy_model(V, H, F, seed=11)
+    toks = np.arange(V)
+    lg = oracle.toy_logits(m["embedding"], m["w_gate"], m["w_up"], m["w_down"], m["w_head"], V, H, F, toks)
+    nxt, margin = oracle.greedy_next_table(lg)
+    # the LM head's error bound on the GPU: its GEMV bar (1e-5 of sum |w x|)
+    # plus the decode layer's output error carried through |W_head|, taken
+    # here as ten times the bar
+    xo, _ = oracle.mlp_layer(m["w_gate"], m["w_up"], m["w_down"], H, F, m["embedding"][toks])
+    _, bound = oracle.q8_gemv(m["w_head"], V, H, xo.astype(np.float32))
+    tol = 1e-4 * bound.max(axis=1)
+    dev = {k: torch.from_numpy(np.ascontiguousarray(m[k])).cuda()
+           for k in ("embedding", "w_gate", "w_up", "w_down", "w_head")}
+    return dev, nxt, margin, tol
+
+
+def orbit(nxt, first):
+    seen, t = [], first
+    while t not in seen:
+        seen.append(t)
+        t = int(nxt[t])
+    return seen
+
+
+def run_gpu(dev, n, first, steps, capacity=None):
+    tokens, count, accept = pti.selfspec_greedy(dev["embedding"], dev["w_gate"], dev["w_up"], dev["w_down"],
+                                                dev["w_head"], V, H, F, n, first, steps, capacity=capacity)
+    torch.cuda.synchronize()
+    return tokens.cpu().numpy(), int(count.item()), accept.cpu().numpy()
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4])
+@pytest.mark.parametrize("first", [0, 7, 13, 300])  # 13 reaches the fixed point 211
+def test_selfspec_matches_the_oracle(toy, n, first):
+    dev, nxt, margin, tol = toy
+    ob = orbit(nxt, first)
+    assert np.all(margin[ob] > tol[ob]), "toy model has a near-tie on this orbit: pick another seed"
+    steps = 40
+    ref_tokens, ref_accept = oracle.selfspec_greedy(nxt, n, first, steps)
+    tokens, count, accept = run_gpu(dev, n, first, steps)
+    assert count == ref_tokens.size
+    np.testing.assert_array_equal(accept, ref_accept)
+    np.testing.assert_array_equal(tokens[:count], ref_tokens)
+    if n == 1:
+        assert np.all(accept == 0)
+    if first == 13 and n > 1:
+        assert accept[-1] == n - 1  # on the fixed point every guess is accepted
+
+
+def test_selfspec_capacity_and_repeat(toy):
+    dev, nxt, _, _ = toy
+    ref_tokens, _ = oracle.selfspec_greedy(nxt, 4, 7, 30)
+    tokens, count, _ = run_gpu(dev, 4, 7, 30, capacity=5)
+    assert count == ref_tokens.size and tokens.size == 5
+    np.testing.assert_array_equal(tokens, ref_tokens[:5])
+    # bit-reproducible run to run (the window and count are reset per call)
+    again = run_gpu(dev, 4, 7, 30)
+    first = run_gpu(dev, 4, 7, 30)
+    np.testing.assert_array_equal(again[0], first[0])
+    assert again[1] == first[1]
+
+
+def test_selfspec_zero_steps(toy):
+    dev, _, _, _ = toy
+    tokens, count, accept = run_gpu(dev, 3, 1, 0)
+    assert count == 0
