@@ -458,6 +458,84 @@ class DecodePass(Q8Pass):
         return run, b, f"oracle mlp_layer: one {hidden}x{ffn} layer (gate, up, down), N={self.n}"
 
 
+class SelfSpecLoop(Q8Pass):
+    """The device-resident greedy self-speculative loop on a toy model at the
+    pages' Qwen3.6-27B shapes (vocab 151936, hidden 5120, ffn 17408): per loop
+    step the embedding gather, one decode layer, the LM head and greedy verify
+    for N streams.  One bench step = one call running `loop_steps` steps."""
+    sources = DECODE_SOURCES + ("pti_verify.cu", "pti_selfspec.cu")
+
+    def __init__(self, vocab=151936, hidden=5120, ffn=17408, n=4, loop_steps=16, seed=0):
+        import torch
+        import pti_synth
+        import stream_quantized_gemv_gb300 as pti
+        self.pti, self.torch = pti, torch
+        self.vocab, self.hidden, self.ffn, self.n, self.loop_steps = vocab, hidden, ffn, n, loop_steps
+        self.name = f"selfspec_greedy_n{n}_{vocab}x{hidden}x{ffn}_x{loop_steps}"
+        self.emb = pti_synth.activations_device(vocab, hidden, seed, 40)
+        self.wg = pti_synth.q8_matrix_device(ffn, hidden, seed, 41)
+        self.wu = pti_synth.q8_matrix_device(ffn, hidden, seed, 42)
+        self.wd = pti_synth.q8_matrix_device(hidden, ffn, seed, 43)
+        self.wh = pti_synth.q8_matrix_device(vocab, hidden, seed, 44)
+        need = pti.selfspec_greedy_workspace_bytes(vocab, hidden, ffn, n)
+        self.ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+        self.out = (torch.zeros(loop_steps * n, dtype=torch.int32, device="cuda"),
+                    torch.zeros(1, dtype=torch.int32, device="cuda"),
+                    torch.zeros(loop_steps, dtype=torch.int32, device="cuda"))
+        layer = 3 * ffn * (hidden // 32) * Q8_BLOCK
+        head = vocab * (hidden // 32) * Q8_BLOCK
+        # algorithmic bytes of a loop step: every weight once, the N embedding
+        # rows, the layer's and the head's activations, the logits written by
+        # the head and read by verify
+        act = 4 * n * (hidden + 2 * (hidden + ffn) + hidden) + 4 * n * 2 * hidden
+        self.weight_bytes = layer + head
+        self.step_bytes = loop_steps * (layer + head + act + 2 * 4 * n * vocab)
+        # per loop step: gather, gate/up + combine, down + combine, RMS,
+        # head + combine, argmax, verify rule + window update; one window init per call
+        self.launches_per_step = 10 * loop_steps + 1
+        self.gemv_launches_per_step = 3 * loop_steps
+        self.launch_bytes = self.step_bytes / self.gemv_launches_per_step
+        self.step()
+        torch.cuda.synchronize()
+        self.tokens_per_step = int(self.out[1].item())   # confirmed tokens per call
+        self.dominant = f"gemv_tma_kernel<Q8,{n}> (LM head {vocab}x{hidden} and the layer's GEMVs)"
+        self.dtype = "f32"
+
+    def step(self, x=None, y=None):
+        self.pti.selfspec_greedy(self.emb, self.wg, self.wu, self.wd, self.wh, self.vocab, self.hidden, self.ffn,
+                                 self.n, 7, self.loop_steps, ws=self.ws, out=self.out)
+
+    def e2e_buffers(self):
+        # the first token is a scalar argument: nothing to copy in; the
+        # confirmed tokens and their count come back
+        t = self.torch
+        hy = t.empty_like(self.out[0], device="cpu").pin_memory()
+        return None, hy, None, self.out[0]
+
+    def config(self):
+        return {"workload": f"greedy self-speculative loop, N={self.n} streams, {self.loop_steps} loop steps per "
+                            f"call, toy model at vocab {self.vocab}, hidden {self.hidden}, ffn {self.ffn}: fp32 "
+                            "embedding, one Q8 gated-MLP layer, Q8 LM head, random weights (about one confirmed "
+                            "token per loop step: the window rarely holds the model's continuation)",
+                "confirmed_tokens_per_call": self.tokens_per_step,
+                "weight_bytes_per_loop_step": self.weight_bytes,
+                "l2": f"inputs larger than L2: {self.weight_bytes / 1e9:.2f} GB of weights per loop step"}
+
+    def cpu_sample(self):
+        import numpy as np
+        import oracle
+        import pti_synth
+        vocab, hidden, ffn = 4096, 1024, 3584   # the same structure at a fifth of the width
+        m = pti_synth.toy_model(vocab, hidden, ffn, seed=0)
+        toks = np.arange(self.n) * 5
+        b = 3 * ffn * (hidden // 32) * Q8_BLOCK + vocab * (hidden // 32) * Q8_BLOCK
+
+        def run():
+            oracle.toy_logits(m["embedding"], m["w_gate"], m["w_up"], m["w_down"], m["w_head"], vocab, hidden,
+                              ffn, toks)
+        return run, b, f"oracle toy_logits of {self.n} window tokens, vocab {vocab}, hidden {hidden}, ffn {ffn}"
+
+
 WORKLOADS = {
     "decode": lambda a: DecodePass(a.cols or 5120, a.rows or 17408, a.n, a.layers or 64),
     "q8": lambda a: Q8Pass(a.rows or 17408, a.cols or 5120, a.n, a.layers or 16),
@@ -465,6 +543,7 @@ WORKLOADS = {
     "twin2": lambda a: TwinPass(a.rows or 17408, a.cols or 5120, a.layers or 8, per_model=2),
     "verify": lambda a: VerifyBatch(steps=a.vsteps),
     "verify_sample": lambda a: VerifySampleBatch(steps=a.vsteps),
+    "selfspec": lambda a: SelfSpecLoop(n=a.n, loop_steps=a.layers or 16),
 }
 
 
@@ -525,7 +604,7 @@ def time_e2e(wl, steps, warmup):
         hy, dy = pinned(wl.out[2]), wl.out[2]
     else:
         hx, hy, dx, dy = wl.e2e_buffers()
-        ins = [(hx, dx)]
+        ins = [] if hx is None else [(hx, dx)]
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         for h, d in ins:
@@ -661,9 +740,13 @@ class _CpuOnly:
 def _cpu_only_workload(name, a):
     """The workload's config and CPU sample without allocating device memory."""
     cls = {"decode": DecodePass, "q8": Q8Pass, "twin": TwinPass, "twin2": TwinPass, "verify": VerifyBatch,
-           "verify_sample": VerifySampleBatch}[name]
+           "verify_sample": VerifySampleBatch, "selfspec": SelfSpecLoop}[name]
     wl = cls.__new__(cls)
-    if name == "decode":
+    if name == "selfspec":
+        wl.vocab, wl.hidden, wl.ffn, wl.n, wl.loop_steps = 151936, 5120, 17408, a.n, a.layers or 16
+        wl.weight_bytes = 3 * wl.ffn * (wl.hidden // 32) * Q8_BLOCK + wl.vocab * (wl.hidden // 32) * Q8_BLOCK
+        wl.tokens_per_step = None
+    elif name == "decode":
         wl.hidden, wl.ffn, wl.n, wl.layers = a.cols or 5120, a.rows or 17408, a.n, a.layers or 64
         wl.weight_bytes = 3 * wl.ffn * (wl.hidden // 32) * Q8_BLOCK
     elif name == "q8":

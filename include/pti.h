@@ -359,7 +359,8 @@ pti_status pti_mlp_decode_pass_ex(const void *const *w_gate, const void *const *
  *     a[i]  = argmax (lowest index on ties) of the model's logits for token
  *             win[i], i.e. the model's next token after win[i];
  *     L     = the number of leading i < n_streams - 1 with win[i+1] == a[i]
- *             (exactly pti_verify_greedy's accepted length, guess = win);
+ *             (pti_verify_greedy's rule with guess = win; argmax ties go to
+ *             the lowest index, -0.0 ties +0.0);
  *     a[0 .. L] are appended to the confirmed text (each is the model's
  *     greedy continuation of a confirmed token, so the text is exactly the
  *     model's greedy rollout from first_token: no quality loss);
@@ -381,8 +382,10 @@ pti_status pti_mlp_decode_pass_ex(const void *const *w_gate, const void *const *
  *   n_streams  1..4 (1: plain greedy decoding, one token per step).
  *   first_token  in [0, vocab).
  *   steps      >= 0 decode steps, each one pass over the weights for all
- *              streams; enqueued as 6 launches per step, no host
- *              synchronisation.
+ *              streams; enqueued as 10 launches per step (embedding gather,
+ *              the decode layer's 5, the LM head and its tile combine, a
+ *              vocabulary-parallel argmax, the verify rule and window
+ *              update), no host synchronisation.
  *   tokens_out DEVICE [tokens_capacity] int32: the confirmed tokens after
  *              first_token, in order; tokens past the capacity are counted
  *              but not stored.

@@ -322,18 +322,25 @@ def selfspec_greedy_workspace_bytes(vocab: int, hidden: int, ffn: int, n_streams
 
 
 def selfspec_greedy(embedding, w_gate, w_up, w_down, w_head, vocab: int, hidden: int, ffn: int, n_streams: int,
-                    first_token: int, steps: int, eps: float = 1e-6, capacity=None, ws=None, stream=None):
+                    first_token: int, steps: int, eps: float = 1e-6, capacity=None, ws=None, stream=None,
+                    out=None):
     """Greedy self-speculative decoding of the toy model on ``n_streams``
     streams for ``steps`` steps, resident on the device.  Returns
     ``(tokens, count, accept)``: the confirmed-token buffer [capacity] int32
     (default steps * n_streams), the device count [1] and the accepted
-    length of every step [steps], all device tensors."""
+    length of every step [steps], all device tensors (``out`` may supply
+    them: int32 tensors of at least those sizes)."""
     import torch
     dev = embedding.device
     cap = steps * n_streams if capacity is None else capacity
-    tokens = torch.zeros(max(cap, 1), dtype=torch.int32, device=dev)
-    count = torch.zeros(1, dtype=torch.int32, device=dev)
-    accept = torch.zeros(max(steps, 1), dtype=torch.int32, device=dev)
+    if out is None:
+        tokens = torch.zeros(max(cap, 1), dtype=torch.int32, device=dev)
+        count = torch.zeros(1, dtype=torch.int32, device=dev)
+        accept = torch.zeros(max(steps, 1), dtype=torch.int32, device=dev)
+    else:
+        tokens, count, accept = out
+        if tokens.numel() < cap or count.numel() < 1 or accept.numel() < steps:
+            raise ValueError("selfspec_greedy: output buffers too small")
     need = selfspec_greedy_workspace_bytes(vocab, hidden, ffn, n_streams)
     if ws is None:
         ws = workspace(need, dev)

@@ -5,12 +5,16 @@
 // outputs, extend the confirmed text with the accepted guesses, restart the
 // rejected streams), read as a window of positions updated in place.
 //
-// One step is six launches in one CUDA stream: the embedding gather, the
-// decode layer (two GEMVs with their tile combines and the final RMS kernel,
-// pti_mlp_decode_pass), the LM-head GEMV (pti_q8_gemv_nstream), greedy verify
-// (pti_verify_greedy) and the window update below.  The window and the
-// confirmed text stay in device memory, so steps are enqueued back to back
-// without a host round trip.
+// One step is, in one CUDA stream: the embedding gather, the decode layer
+// (two GEMVs with their tile combines and the final RMS kernel,
+// pti_mlp_decode_pass), the LM-head GEMV (pti_q8_gemv_nstream, with its tile
+// combine), the greedy verify of the step and the window update below.  The
+// verify is split in two: a vocabulary-parallel argmax (a single step's
+// 4 x vocab logits are too few rows for pti_verify_greedy's one CTA per step
+// to stream them fast) and the match / accepted-length rule in the update
+// kernel, with pti_verify_greedy's semantics.  The window and the confirmed
+// text stay in device memory, so steps are enqueued back to back without a
+// host round trip.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -23,15 +27,59 @@ namespace pti {
 namespace {
 
 constexpr int kGatherThreads = 256;
+constexpr int kArgmaxThreads = 256;
+constexpr int kArgmaxChunk = 4096;  // logits of one stream per argmax CTA
+
+// Orderable 64-bit key of (value, index): the float's bits mapped to an
+// unsigned integer with the same order (-0.0 folded onto +0.0, so the two
+// tie), above the complement of the index, so the maximum key is the largest
+// value and, among equal values, the lowest index.  The maximum of keys does
+// not depend on the order they are combined in.
+__device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) {
+  uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<unsigned long long>(u) << 32) | (0xFFFFFFFFu - idx);
+}
+
+// keys[s] = max over v of argmax_key(logits[s][v], v); keys start at 0 (below
+// every key), reset by the gather kernel of the step.
+__global__ void __launch_bounds__(kArgmaxThreads) argmax_split_kernel(const float *__restrict__ logits,
+                                                                      int64_t vocab,
+                                                                      unsigned long long *__restrict__ keys) {
+  const int s = static_cast<int>(blockIdx.y);
+  const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kArgmaxChunk;
+  const int64_t v1 = v0 + kArgmaxChunk < vocab ? v0 + kArgmaxChunk : vocab;
+  const float *row = logits + static_cast<int64_t>(s) * vocab;
+  unsigned long long best = 0ull;
+  for (int64_t v = v0 + threadIdx.x; v < v1; v += kArgmaxThreads) {
+    const unsigned long long k = argmax_key(__ldcs(row + v), static_cast<uint32_t>(v));
+    best = k > best ? k : best;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long k = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+    best = k > best ? k : best;
+  }
+  __shared__ unsigned long long warp_best[kArgmaxThreads / 32];
+  if ((threadIdx.x & 31u) == 0) warp_best[threadIdx.x >> 5] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kArgmaxThreads / 32; ++w) best = warp_best[w] > best ? warp_best[w] : best;
+    atomicMax(keys + s, best);
+  }
+}
 
 // x[s][:] = embedding[win[s]][:] for the n streams (the token clamped to
-// [0, vocab), so a corrupt window cannot index outside the table).
+// [0, vocab), so a corrupt window cannot index outside the table); also
+// resets the step's argmax keys.
 __global__ void __launch_bounds__(kGatherThreads) embed_gather_kernel(const float *__restrict__ emb,
                                                                       const int32_t *__restrict__ win, int n,
                                                                       int64_t vocab, int64_t hidden,
-                                                                      float *__restrict__ x) {
+                                                                      float *__restrict__ x,
+                                                                      unsigned long long *__restrict__ keys) {
   const int s = static_cast<int>(blockIdx.y);
   if (s >= n) return;
+  if (blockIdx.x == 0 && threadIdx.x == 0) keys[s] = 0ull;
   int64_t t = win[s];
   t = t < 0 ? 0 : (t >= vocab ? vocab - 1 : t);
   const float4 *src = reinterpret_cast<const float4 *>(emb + t * hidden);
@@ -41,14 +89,15 @@ __global__ void __launch_bounds__(kGatherThreads) embed_gather_kernel(const floa
     dst[i] = src[i];
 }
 
-// The window update after verify: the accepted length L and the argmax a[]
-// of the step give the confirmed tokens a[0 .. L] and the next window
+// The verify rule and the window update: a[s] = the argmax of stream s (from
+// its key), L = the number of leading s < n - 1 with win[s + 1] == a[s] (the
+// guess fed to stream s + 1 is what stream s produced: pti_verify_greedy's
+// accepted length), then the confirmed tokens a[0 .. L] and the next window
 // win[0] = a[L], win[j] = a[L + j] (or a[n - 1] past the end).
 struct UpdateArgs {
-  int32_t *win;              // [n] the window (stream inputs)
-  const int32_t *argmax;     // [n]
-  const int32_t *accept;     // [1]
-  int32_t *tokens;           // [capacity] confirmed text
+  int32_t *win;                   // [n] the window (stream inputs)
+  const unsigned long long *keys; // [n] argmax keys of the step
+  int32_t *tokens;                // [capacity] confirmed text
   int64_t capacity;
   int32_t *count;            // [1] confirmed tokens so far
   int32_t *accept_log;       // [steps] or null
@@ -58,9 +107,9 @@ struct UpdateArgs {
 __global__ void __launch_bounds__(32) window_update_kernel(const UpdateArgs u) {
   if (threadIdx.x != 0) return;
   int32_t a[4];
-  for (int i = 0; i < u.n; ++i) a[i] = u.argmax[i];
-  int L = u.accept[0];
-  L = L < 0 ? 0 : (L > u.n - 1 ? u.n - 1 : L);
+  for (int i = 0; i < u.n; ++i) a[i] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(u.keys[i]));
+  int L = 0;
+  while (L < u.n - 1 && u.win[L + 1] == a[L]) ++L;
   const int32_t c = u.count[0];
   for (int i = 0; i <= L; ++i)
     if (static_cast<int64_t>(c) + i < u.capacity) u.tokens[c + i] = a[i];
@@ -76,10 +125,10 @@ __global__ void __launch_bounds__(32) window_init_kernel(int32_t *win, int n, in
 
 size_t round256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
-// Workspace: window, argmax, match, accept, x, y, logits, then the decode
-// pass's and the LM-head GEMV's own workspaces.
+// Workspace: window, argmax keys, x, y, logits, then the decode pass's and
+// the LM-head GEMV's own workspaces.
 struct SelfspecLayout {
-  size_t win = 0, argmax = 0, match = 0, accept = 0, x = 0, y = 0, logits = 0, decode = 0, gemv = 0, total = 0;
+  size_t win = 0, keys = 0, x = 0, y = 0, logits = 0, decode = 0, gemv = 0, total = 0;
   size_t decode_bytes = 0, gemv_bytes = 0;
 };
 
@@ -88,12 +137,8 @@ SelfspecLayout selfspec_layout(int64_t vocab, int64_t hidden, int64_t ffn, int n
   size_t off = 0;
   d.win = off;
   off = round256(off + 4 * sizeof(int32_t));
-  d.argmax = off;
-  off = round256(off + 4 * sizeof(int32_t));
-  d.match = off;
-  off = round256(off + 4);
-  d.accept = off;
-  off = round256(off + sizeof(int32_t));
+  d.keys = off;
+  off = round256(off + 4 * sizeof(unsigned long long));
   d.x = off;
   off = round256(off + static_cast<size_t>(n) * hidden * sizeof(float));
   d.y = off;
@@ -177,9 +222,7 @@ extern "C" pti_status pti_selfspec_greedy(const pti_toy_model *model, int n_stre
   const SelfspecLayout d = selfspec_layout(model->vocab, model->hidden, model->ffn, n_streams);
   uint8_t *const ws = static_cast<uint8_t *>(workspace);
   int32_t *const win = reinterpret_cast<int32_t *>(ws + d.win);
-  int32_t *const argmax = reinterpret_cast<int32_t *>(ws + d.argmax);
-  uint8_t *const match = ws + d.match;
-  int32_t *const accept = reinterpret_cast<int32_t *>(ws + d.accept);
+  unsigned long long *const keys = reinterpret_cast<unsigned long long *>(ws + d.keys);
   float *const x = reinterpret_cast<float *>(ws + d.x);
   float *const y = reinterpret_cast<float *>(ws + d.y);
   float *const logits = reinterpret_cast<float *>(ws + d.logits);
@@ -189,12 +232,13 @@ extern "C" pti_status pti_selfspec_greedy(const pti_toy_model *model, int n_stre
   if (cudaGetLastError() != cudaSuccess) return PTI_ERR_CUDA;
   const int64_t chunks = model->hidden / 4;
   const unsigned gx = static_cast<unsigned>((chunks + kGatherThreads - 1) / kGatherThreads);
+  const unsigned ax = static_cast<unsigned>((model->vocab + kArgmaxChunk - 1) / kArgmaxChunk);
   const void *const wg[1] = {model->w_gate};
   const void *const wu[1] = {model->w_up};
   const void *const wd[1] = {model->w_down};
   for (int step = 0; step < steps; ++step) {
     embed_gather_kernel<<<dim3(gx, static_cast<unsigned>(n_streams)), kGatherThreads, 0, st>>>(
-        model->embedding, win, n_streams, model->vocab, model->hidden, x);
+        model->embedding, win, n_streams, model->vocab, model->hidden, x, keys);
     if (cudaGetLastError() != cudaSuccess) return PTI_ERR_CUDA;
     if (const pti_status s = pti_mlp_decode_pass(wg, wu, wd, 1, model->hidden, model->ffn, n_streams, model->eps,
                                                  x, y, ws + d.decode, d.decode_bytes, stream);
@@ -204,11 +248,10 @@ extern "C" pti_status pti_selfspec_greedy(const pti_toy_model *model, int n_stre
                                                  ws + d.gemv, d.gemv_bytes, stream);
         s != PTI_OK)
       return s;
-    if (const pti_status s = pti_verify_greedy(logits, win, 1, n_streams, model->vocab, argmax,
-                                               n_streams > 1 ? match : nullptr, accept, stream);
-        s != PTI_OK)
-      return s;
-    UpdateArgs u{win, argmax, accept, tokens_out, tokens_capacity, count_out, accept_out, step, n_streams};
+    argmax_split_kernel<<<dim3(ax, static_cast<unsigned>(n_streams)), kArgmaxThreads, 0, st>>>(logits, model->vocab,
+                                                                                              keys);
+    if (cudaGetLastError() != cudaSuccess) return PTI_ERR_CUDA;
+    UpdateArgs u{win, keys, tokens_out, tokens_capacity, count_out, accept_out, step, n_streams};
     window_update_kernel<<<1, 32, 0, st>>>(u);
     if (cudaGetLastError() != cudaSuccess) return PTI_ERR_CUDA;
   }
