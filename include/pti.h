@@ -381,7 +381,7 @@ pti_status pti_mlp_decode_pass_ex(const void *const *w_gate, const void *const *
  *              eps finite >= 0.
  *   n_streams  1..4 (1: plain greedy decoding, one token per step).
  *   first_token  in [0, vocab).
- *   steps      >= 0 decode steps, each one pass over the weights for all
+ *   steps      0 .. 2^28 decode steps, each one pass over the weights for all
  *              streams; enqueued as 10 launches per step (embedding gather,
  *              the decode layer's 5, the LM head and its tile combine, a
  *              vocabulary-parallel argmax, the verify rule and window
@@ -396,7 +396,9 @@ pti_status pti_mlp_decode_pass_ex(const void *const *w_gate, const void *const *
  *              ffn, n_streams) bytes, 256-byte aligned, scratch.
  * Errors: invalid arguments return a status and enqueue nothing; the embedding
  * and the tokens are checked only on the host side (pointers, alignment);
- * a token is used as an index only after clamping to [0, vocab).
+ * a token is used as an index only after clamping to [0, vocab).  As for
+ * pti_verify_greedy the logits must be finite (a NaN logit makes the argmax
+ * unspecified).
  */
 typedef struct pti_toy_model {
     const float *embedding;

@@ -182,7 +182,8 @@ extern "C" pti_status pti_selfspec_greedy(const pti_toy_model *model, int n_stre
       model->w_down == nullptr || model->w_head == nullptr)
     return PTI_ERR_NULL;
   if (n_streams < 1 || n_streams > 4) return PTI_ERR_NSTREAMS;
-  if (steps < 0 || tokens_capacity < 0 || !valid_model(model)) return PTI_ERR_SHAPE;
+  // steps * n_streams confirmed tokens must fit the int32 count
+  if (steps < 0 || steps > (1 << 28) || tokens_capacity < 0 || !valid_model(model)) return PTI_ERR_SHAPE;
   if (tokens_capacity > 0 && tokens_out == nullptr) return PTI_ERR_NULL;
   if (first_token < 0 || first_token >= model->vocab) return PTI_ERR_VALUE;
   if (!std::isfinite(model->eps) || model->eps < 0.0) return PTI_ERR_VALUE;

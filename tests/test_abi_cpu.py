@@ -231,7 +231,7 @@ def test_selfspec_validation(L):
     assert call(model=_toy(emb=None)) == 1 and call(model=_toy(head=None)) == 1
     assert call(count=None) == 1 and call(w=None) == 1 and call(tokens=None) == 1
     assert call(n=0) == 3 and call(n=5) == 3
-    assert call(steps=-1) == 2 and call(cap=-1) == 2
+    assert call(steps=-1) == 2 and call(steps=(1 << 28) + 1) == 2 and call(cap=-1) == 2
     assert call(model=_toy(vocab=1)) == 2 and call(model=_toy(hidden=100)) == 2
     assert call(first=-1) == 8 and call(first=512) == 8
     assert call(model=_toy(eps=-1.0)) == 8 and call(model=_toy(eps=float("nan"))) == 8
