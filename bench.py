@@ -196,6 +196,8 @@ class Q8Pass:
         self.tokens_per_step = n
         self.dominant = "gemv_tma_kernel<Q8,%d>" % n
         self.dtype = "f32"
+        # FP32 FMA lane-operations: per weight N products and one dequantising FMA
+        self.fma_ops_per_step = layers * rows * cols * (n + 1)
 
     def step(self, x=None, y=None):
         # a chain of GEMVs as in a decode step: every launch after the first
@@ -262,6 +264,8 @@ class TwinPass(Q8Pass):
         self.tokens_per_step = self.n
         self.dominant = f"gemv_tma_kernel<Twin,{per_model}>"
         self.dtype = "f32"
+        # per element two weights (models A and B), each with per_model products and one dequantising FMA
+        self.fma_ops_per_step = layers * rows * cols * 2 * (per_model + 1)
 
     def step(self, x=None, y=None):
         x = self.x if x is None else x
@@ -400,6 +404,7 @@ class VerifySampleBatch(Q8Pass):
 class DecodePass(Q8Pass):
     """The chained decode weight pass: L layers of gate/up/down Q8 GEMVs with
     the fused SiLU and RMS glue, N streams (one step = one pass)."""
+    sources = DECODE_SOURCES
 
     def __init__(self, hidden=5120, ffn=17408, n=4, layers=64, seed=0):
         import torch
@@ -425,6 +430,7 @@ class DecodePass(Q8Pass):
         # then the final RMS kernel
         self.launches_per_step = 4 * layers + 1
         self.gemv_launches_per_step = 2 * layers
+        self.fma_ops_per_step = layers * 3 * ffn * hidden * (n + 1)
         self.tokens_per_step = n
         self.dominant = f"gemv_tma_kernel<Q8,{n},GateUp|Down> (the pass's {2 * layers} GEMV launches)"
         self.dtype = "f32"
@@ -495,6 +501,7 @@ class SelfSpecLoop(Q8Pass):
         self.launches_per_step = 10 * loop_steps + 1
         self.gemv_launches_per_step = 3 * loop_steps
         self.launch_bytes = self.step_bytes / self.gemv_launches_per_step
+        self.fma_ops_per_step = loop_steps * (3 * ffn * hidden + vocab * hidden) * (n + 1)
         self.step()
         torch.cuda.synchronize()
         self.tokens_per_step = int(self.out[1].item())   # confirmed tokens per call
@@ -718,6 +725,20 @@ def main():
                         "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
                 "gpu_launches": wl.launches_per_step * a.steps,
                 "clocks": clocks, "device_error": err}
+        fma_ops = getattr(wl, "fma_ops_per_step", None)
+        if fma_ops:
+            # the 4-stream GEMVs are limited by FP32 arithmetic on the CUDA
+            # cores as much as by HBM: FMA lane-operations per second against
+            # 128 FP32 lanes per SM x SMs x the SM clock sampled under load
+            sms = torch.cuda.get_device_properties(local).multi_processor_count
+            mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or 2070.0
+            fma_peak = 128.0 * sms * mhz * 1e6
+            fma_rate = fma_ops / (ms * 1e-3)
+            line["alu_roofline"] = {"bound": "alu", "kernel": wl.dominant, "unit": "FMA lane-ops/s",
+                                    "achieved": round(fma_rate, 1), "peak": round(fma_peak, 1),
+                                    "frac": round(fma_rate / fma_peak, 4),
+                                    "peak_derivation": f"128 FP32 lanes x {sms} SMs x {mhz:.0f} MHz",
+                                    "ops": "per weight: N product FMAs + 1 dequantising FMA"}
         if rank == 0 and world == 1 and not a.no_cpu_baseline:
             import oracle
             oracle.build()
