@@ -729,8 +729,9 @@ __device__ __forceinline__ void consumer_loop(const GemvArgs &a, const ConsumerC
         c.red[((sl * T::kWarps + c.warp) * kOut + s) * 64 + r * 32 + c.lane] = v.x + v.y;
       }
     if (middle) {
-      // a tile wholly inside this CTA's range: finish it now (rare: only when
-      // a CTA spans more than two row tiles)
+      // a tile wholly inside this CTA's range: finish it now (when a CTA
+      // spans more than two row tiles, as most gate/up CTAs of the decode
+      // pass do: 20 units per tile, about 36 per CTA)
       wait_scales();
       named_barrier(kBarConsumers, kConsumerThreads);
       finish_tiles<F, N, E>(a, c.red, 1, rb, 1, 0, 0, c.tid, c.flag, c.epi);
