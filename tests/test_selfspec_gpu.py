@@ -93,9 +93,8 @@ def test_selfspec_zero_steps(toy):
 def test_selfspec_large_model_matches_the_oracle_on_its_orbit():
     """A larger toy model (vocab 12296: a ragged last LM-head tile and a ragged
     last argmax chunk; hidden 2048, ffn 5632: tiles shared by several CTAs in
-    every GEMV; the decode layer at the bench's shapes is covered by the
-    decode-pass tests, and the fp64 oracle would need minutes per token
-    there), N = 4, from device-generated weights copied back: the oracle
+    every GEMV; the benchmark's shapes have their own test below, with fewer
+    loop steps), N = 4, from device-generated weights copied back: the oracle
     evaluates the model only on the tokens the loop can feed it (the first
     token's orbit under the greedy map); tokens, count and accepted lengths
     must match."""
@@ -134,6 +133,54 @@ def test_selfspec_large_model_matches_the_oracle_on_its_orbit():
     table = np.zeros(Vf, dtype=np.int32)
     for a, b in zip(toks, toks[1:] + [last]):
         table[a] = b
+    ref_tokens, ref_accept = oracle.selfspec_greedy(table, n, first, steps)
+    tokens, count, accept = pti.selfspec_greedy(emb, wg, wu, wd, wh, Vf, Hf, Ff, n, first, steps)
+    torch.cuda.synchronize()
+    assert int(count.item()) == ref_tokens.size
+    np.testing.assert_array_equal(accept.cpu().numpy(), ref_accept)
+    np.testing.assert_array_equal(tokens.cpu().numpy()[:ref_tokens.size], ref_tokens)
+
+
+def test_selfspec_at_the_bench_shapes_matches_the_oracle_on_its_orbit():
+    """The loop at the shapes the benchmark times (vocab 151936, hidden 5120,
+    ffn 17408, N = 4, the benchmark's device-generated tensors and first
+    token), two loop steps.  With a window that holds one token in every
+    stream the loop feeds the model only the first token's orbit under the
+    greedy map (one new token per step, or a fixed point), so two steps need
+    the greedy next token of the first two orbit tokens: the oracle evaluates
+    the model on those (an fp64 LM head of 151936 x 5120 each).  Every other
+    entry of the oracle's table maps a token to itself: an entry the loop used
+    without it being right would put a self-loop into the oracle's tokens that
+    the model does not have, so equal outputs mean no such entry was used."""
+    Vf, Hf, Ff, n, steps = 151936, 5120, 17408, 4, 2
+    emb = pti_synth.activations_device(Vf, Hf, 0, 40)
+    wg = pti_synth.q8_matrix_device(Ff, Hf, 0, 41)
+    wu = pti_synth.q8_matrix_device(Ff, Hf, 0, 42)
+    wd = pti_synth.q8_matrix_device(Hf, Ff, 0, 43)
+    wh = pti_synth.q8_matrix_device(Vf, Hf, 0, 44)
+    h_wg, h_wu, h_wd, h_wh = (t.cpu().numpy() for t in (wg, wu, wd, wh))
+
+    def greedy_next(t):
+        row = emb[t:t + 1].cpu().numpy()
+        xo, _ = oracle.mlp_layer(h_wg, h_wu, h_wd, Hf, Ff, row)
+        hi = xo.astype(np.float32)
+        lo = (xo - hi.astype(np.float64)).astype(np.float32)
+        y, b = oracle.q8_gemv(h_wh, Vf, Hf, np.concatenate([hi, lo]))
+        nxt, margin = oracle.greedy_next_table((y[0] + y[1])[None, :])
+        return int(nxt[0]), margin[0] > 1e-4 * b[0].max()
+
+    for first in (7, 100, 2000):  # 7 is the benchmark's first token
+        table = np.arange(Vf, dtype=np.int32)
+        t, clear = first, True
+        for _ in range(steps):
+            nxt, ok = greedy_next(t)
+            clear = clear and ok
+            table[t] = nxt
+            t = nxt
+        if clear:
+            break
+    else:
+        pytest.fail("no start token with a clear orbit")
     ref_tokens, ref_accept = oracle.selfspec_greedy(table, n, first, steps)
     tokens, count, accept = pti.selfspec_greedy(emb, wg, wu, wd, wh, Vf, Hf, Ff, n, first, steps)
     torch.cuda.synchronize()
