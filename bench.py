@@ -406,14 +406,13 @@ class DecodePass(Q8Pass):
     the fused SiLU and RMS glue, N streams (one step = one pass)."""
     sources = DECODE_SOURCES
 
-    def __init__(self, hidden=5120, ffn=17408, n=4, layers=64, seed=0, persistent=False):
+    def __init__(self, hidden=5120, ffn=17408, n=4, layers=64, seed=0):
         import torch
         import pti_synth
         import stream_quantized_gemv_gb300 as pti
         self.pti, self.torch = pti, torch
         self.hidden, self.ffn, self.n, self.layers = hidden, ffn, n, layers
-        self.persistent = persistent
-        self.name = f"mlp_decode_pass_n{n}_{hidden}x{ffn}_x{layers}" + ("_persistent" if persistent else "")
+        self.name = f"mlp_decode_pass_n{n}_{hidden}x{ffn}_x{layers}"
         gate = [pti_synth.q8_matrix_device(ffn, hidden, seed, 3 * l) for l in range(layers)]
         up = [pti_synth.q8_matrix_device(ffn, hidden, seed, 3 * l + 1) for l in range(layers)]
         down = [pti_synth.q8_matrix_device(hidden, ffn, seed, 3 * l + 2) for l in range(layers)]
@@ -430,8 +429,6 @@ class DecodePass(Q8Pass):
         # per layer: gate/up GEMV, its tile combine, down GEMV, its tile combine;
         # then the final RMS kernel
         self.launches_per_step = 4 * layers + 1
-        if persistent:  # one cooperative launch per 64 layers, then the final RMS kernel
-            self.launches_per_step = (layers + 63) // 64 + 1
         self.gemv_launches_per_step = 2 * layers
         self.fma_ops_per_step = layers * 3 * ffn * hidden * (n + 1)
         self.tokens_per_step = n
@@ -441,8 +438,7 @@ class DecodePass(Q8Pass):
     def step(self, x=None, y=None):
         x = self.x if x is None else x
         y = self.y if y is None else y
-        self.pti.mlp_decode_pass(self.weights, self.hidden, self.ffn, x, x_out=y, ws=self.ws,
-                                 persistent=self.persistent)
+        self.pti.mlp_decode_pass(self.weights, self.hidden, self.ffn, x, x_out=y, ws=self.ws)
 
     def config(self):
         return {"workload": f"{self.layers}-layer decode weight pass, N={self.n} fp32 streams: per layer Q8 gate "
@@ -548,7 +544,7 @@ class SelfSpecLoop(Q8Pass):
 
 
 WORKLOADS = {
-    "decode": lambda a: DecodePass(a.cols or 5120, a.rows or 17408, a.n, a.layers or 64, persistent=a.persistent),
+    "decode": lambda a: DecodePass(a.cols or 5120, a.rows or 17408, a.n, a.layers or 64),
     "q8": lambda a: Q8Pass(a.rows or 17408, a.cols or 5120, a.n, a.layers or 16),
     "twin": lambda a: TwinPass(a.rows or 17408, a.cols or 5120, a.layers or 8),
     "twin2": lambda a: TwinPass(a.rows or 17408, a.cols or 5120, a.layers or 8, per_model=2),
@@ -665,8 +661,6 @@ def main():
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--vsteps", type=int, default=4096, help="steps of the verify batches")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--persistent", action="store_true",
-                    help="decode pass: one persistent cooperative launch per 64 layers instead of chained launches")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
 

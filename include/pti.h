@@ -148,9 +148,11 @@ pti_status pti_q8_gemv_nstream_ex(const void *w_q8, int64_t rows, int64_t cols, 
  * depends only on n_streams, at most 1.31 MB); a request for more would return
  * PTI_ERR_WORKSPACE before anything is enqueued.  The call allocates nothing.
  *
- * The first call on a device looks up the array's device address.  All calls
- * on a device share the one array: calls that overlap on the GPU race, so
- * order them (one stream, or synchronise).
+ * The first call on a device looks up the array's device address (so make
+ * that first call before any stream capture) and keeps it for the life of the
+ * process: do not use this entry point across a cudaDeviceReset of that
+ * device.  All calls on a device share the one array: calls that overlap on
+ * the GPU race, so order them (one stream, or synchronise).
  */
 size_t pti_q8_gemv_noalloc_max_scratch_bytes(void);
 
@@ -159,9 +161,13 @@ pti_status pti_q8_gemv_nstream_noalloc(const void *w_q8, int64_t rows, int64_t c
 
 /*
  * SSQ mode-16 twin GEMV.
- *   [PTI-readme] §"与 SSQ（Side-by-Side Quantization）的关系": per uint16 pw,
- *   wa = (int8)(pw >> 8), wb = (int8)(pw & 0xFF); acc_a += scale_a*wa*x_a[i],
- *   acc_b += scale_b*wb*x_b[i]: one memory transaction, two compute streams.
+ *   [PTI-readme] §"与 SSQ（Side-by-Side Quantization）的关系" and [PTI-forum]
+ *   §"PTI的核心创新：SSQ打包技术": a twin block packs the same 32 columns of
+ *   two models.  It starts with model A's binary16 scale and then model B's,
+ *   followed by 32 little-endian 16-bit elements; element i holds column i
+ *   of model A as a signed byte in its upper 8 bits and column i of model B
+ *   in its lower 8 bits.  One read of the packed matrix gives both products,
+ *   y_a = W_A x_a and y_b = W_B x_b.
  *
  *   w_twin     [rows][cols/32] twin blocks (68 bytes each), 16-byte aligned.
  *   rows, cols as for the Q8 GEMV.
@@ -308,9 +314,11 @@ pti_status pti_verify_sample(const float *logits, const int32_t *guess, const fl
  * streams W_down and applies h's RMS scale to its output; each writes per-tile
  * sums of squares of its output, from which the next step takes the RMS scale
  * of its input (W (c v) = c (W v), so no separate normalisation pass over the
- * vectors is needed).  A last kernel applies the final RMS scale.  How the
- * steps are launched: see pti_mlp_decode_pass_ex.  The first launch waits for
- * all earlier work in the stream.
+ * vectors is needed).  A last kernel applies the final RMS scale.  Each
+ * gate/up and down step is its own launch (with a small kernel behind it that
+ * combines the row tiles several CTAs shared), all chained by programmatic
+ * dependent launch: a step streams its first weight tiles while the previous
+ * one finishes.  The first launch waits for all earlier work in the stream.
  * Arithmetic: GEMVs as in the conventions, SiLU with expf, RMS scales from
  * fp32 per-tile sums of squares summed exactly enough (float-float, about
  * 1e-15 relative) and a float reciprocal square root refined in double;
@@ -323,28 +331,6 @@ pti_status pti_mlp_decode_pass(const void *const *w_gate, const void *const *w_u
                                const float *x_in, float *x_out,
                                void *workspace, size_t workspace_bytes,
                                pti_stream_t stream);
-
-/*
- * pti_mlp_decode_pass with flags.  By default (flags 0) each gate/up and down
- * step is its own launch, 2 n_layers + 1 launches chained by programmatic
- * dependent launch.
- *   PTI_FLAG_DECODE_PERSISTENT  run the steps in persistent cooperative
- *                launches of up to 64 layers each instead (one CTA per SM, a
- *                grid barrier between steps, the next step's weights streamed
- *                in while the grid crosses the barrier), then the final
- *                kernel; if the device cannot run a cooperative grid of one
- *                CTA per SM the call returns PTI_ERR_CUDA and enqueues
- *                nothing.
- * Other flag bits return PTI_ERR_VALUE.  Same arguments and results
- * otherwise; the two forms differ only in rounding order.
- */
-#define PTI_FLAG_DECODE_PERSISTENT 0x2u
-
-pti_status pti_mlp_decode_pass_ex(const void *const *w_gate, const void *const *w_up, const void *const *w_down,
-                                  int n_layers, int64_t hidden, int64_t ffn, int n_streams, double eps,
-                                  const float *x_in, float *x_out,
-                                  void *workspace, size_t workspace_bytes,
-                                  pti_stream_t stream, uint32_t flags);
 
 /*
  * Greedy self-speculative decoding of a toy model, on the device.
@@ -413,6 +399,30 @@ pti_status pti_selfspec_greedy(const pti_toy_model *model, int n_streams, int32_
                                int32_t *tokens_out, int64_t tokens_capacity, int32_t *count_out,
                                int32_t *accept_out, void *workspace, size_t workspace_bytes,
                                pti_stream_t stream);
+
+/*
+ * Testing hook for the pipeline's bounded waits; the pages have no
+ * counterpart.  It is the fast-path pti_q8_gemv_nstream (cols % 256 == 0, x
+ * 16-byte aligned, workspace given) with two changes that make one wait run
+ * out without harming the GPU:
+ *   - the copy producer of the first CTA issues no copy from its unit
+ *     `stall_unit` on, as if that copy never arrived;
+ *   - every pipeline wait gives up after `wait_ns` nanoseconds instead of
+ *     2 seconds.
+ * The consumer warps waiting for the missing tile then give up, record
+ * PTI_DEVERR_FULL_TIMEOUT in the device error word (pti_device_error), and
+ * skip their remaining waits; every copy that was issued has landed before the
+ * kernel exits (else PTI_DEVERR_DRAIN_TIMEOUT is recorded too), so the
+ * device, the stream and the library stay usable.  y is undefined afterwards.
+ *   stall_unit  at least 6 (the ring depth) and below the first CTA's unit
+ *               count (units / grid, units = (rows/128 rounded up) (cols/256),
+ *               grid = min(SM count, units, 320)); else PTI_ERR_VALUE.
+ *   wait_ns     1000 .. 2e9; else PTI_ERR_VALUE.
+ * Other arguments and checks as pti_q8_gemv_nstream.
+ */
+pti_status pti_test_q8_gemv_stall(const void *w_q8, int64_t rows, int64_t cols, int n_streams,
+                                  const float *x, float *y, void *workspace, size_t workspace_bytes,
+                                  pti_stream_t stream, int64_t stall_unit, uint64_t wait_ns);
 
 /*
  * Reads and clears the device error word of the current device (a blocking

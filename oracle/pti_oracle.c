@@ -184,10 +184,11 @@ int pti_or_q8_gemv_rows(const uint8_t *w, int64_t rows, int64_t cols, int n,
 }
 
 /* ---------------------------------------------------------------------------
- * SSQ twin GEMV: acc_a += scale_a * wa * x_a[i] and acc_b += scale_b * wb *
- * x_b[i] from one uint16 per position ([PTI-readme] §"与 SSQ（Side-by-Side
- * Quantization）的关系"; [PTI-forum] §"PTI的核心创新：SSQ打包技术": one memory
- * transaction, two compute streams).
+ * SSQ twin GEMV ([PTI-readme] §"与 SSQ（Side-by-Side Quantization）的关系";
+ * [PTI-forum] §"PTI的核心创新：SSQ打包技术"): y_a[r] is the dot product of model
+ * A's dequantised row (the upper bytes of the packed 16-bit elements times A's
+ * block scales) with x_a, y_b[r] that of model B's row (the lower bytes times
+ * B's scales) with x_b; both come from one read of the packed matrix.
  * ------------------------------------------------------------------------- */
 int pti_or_twin_gemv_rows(const uint8_t *w, int64_t rows, int64_t cols,
                           const float *xa, const float *xb,

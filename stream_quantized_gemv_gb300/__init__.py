@@ -91,13 +91,12 @@ def lib() -> ctypes.CDLL:
             L.pti_mlp_decode_pass_workspace_bytes.argtypes = [I64, I64, I]
             L.pti_mlp_decode_pass.restype = I
             L.pti_mlp_decode_pass.argtypes = [P, P, P, I, I64, I64, I, ctypes.c_double, P, P, P, SZ, P]
-            L.pti_mlp_decode_pass_ex.restype = I
-            L.pti_mlp_decode_pass_ex.argtypes = [P, P, P, I, I64, I64, I, ctypes.c_double, P, P, P, SZ, P,
-                                                 ctypes.c_uint32]
             L.pti_selfspec_greedy_workspace_bytes.restype = SZ
             L.pti_selfspec_greedy_workspace_bytes.argtypes = [I64, I64, I64, I]
             L.pti_selfspec_greedy.restype = I
             L.pti_selfspec_greedy.argtypes = [ctypes.POINTER(ToyModel), I, ctypes.c_int32, I, P, I64, P, P, P, SZ, P]
+            L.pti_test_q8_gemv_stall.restype = I
+            L.pti_test_q8_gemv_stall.argtypes = [P, I64, I64, I, P, P, P, SZ, P, I64, ctypes.c_uint64]
             L.pti_device_error.restype = I
             L.pti_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             _lib = L
@@ -285,15 +284,9 @@ class DecodeWeights:
         self.n_layers = len(w_gate)
 
 
-FLAG_DECODE_PERSISTENT = 0x2
-
-
-def mlp_decode_pass(weights, hidden: int, ffn: int, x, eps: float = 1e-6, x_out=None, ws=None, stream=None,
-                    persistent: bool = False):
+def mlp_decode_pass(weights, hidden: int, ffn: int, x, eps: float = 1e-6, x_out=None, ws=None, stream=None):
     """Runs the gated-MLP layers of ``weights`` (a ``DecodeWeights``) over the
-    streams x [n][hidden] and returns x_out [n][hidden].  ``persistent`` runs
-    the steps in one cooperative launch per 64 layers instead of one launch
-    per step."""
+    streams x [n][hidden] and returns x_out [n][hidden]."""
     import torch
     if x.dim() == 1:
         x = x.unsqueeze(0)
@@ -303,10 +296,10 @@ def mlp_decode_pass(weights, hidden: int, ffn: int, x, eps: float = 1e-6, x_out=
     need = mlp_decode_pass_workspace_bytes(hidden, ffn, n)
     if ws is None:
         ws = workspace(need, x.device)
-    _check(lib().pti_mlp_decode_pass_ex(weights.gate, weights.up, weights.down, weights.n_layers, hidden, ffn, n,
-                                        float(eps), _ptr(x), _ptr(x_out), _ptr(ws),
-                                        0 if ws is None else ws.numel() * ws.element_size(), _stream(stream),
-                                        FLAG_DECODE_PERSISTENT if persistent else 0), "pti_mlp_decode_pass")
+    _check(lib().pti_mlp_decode_pass(weights.gate, weights.up, weights.down, weights.n_layers, hidden, ffn, n,
+                                     float(eps), _ptr(x), _ptr(x_out), _ptr(ws),
+                                     0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+           "pti_mlp_decode_pass")
     return x_out
 
 
@@ -351,6 +344,23 @@ def selfspec_greedy(embedding, w_gate, w_up, w_down, w_head, vocab: int, hidden:
                                      0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
            "pti_selfspec_greedy")
     return tokens[:cap], count, accept[:steps]
+
+
+def test_q8_gemv_stall(w, rows: int, cols: int, x, stall_unit: int, wait_ns: int, y=None, ws=None, stream=None):
+    """The testing hook ``pti_test_q8_gemv_stall``: a fast-path Q8 GEMV whose
+    first CTA stops issuing copies at unit ``stall_unit``, with every pipeline
+    wait bounded by ``wait_ns``.  Returns y (undefined after the stall)."""
+    import torch
+    n = x.shape[0]
+    if y is None:
+        y = torch.empty((n, rows), dtype=torch.float32, device=x.device)
+    need = q8_gemv_workspace_bytes(rows, cols, n)
+    if ws is None:
+        ws = workspace(need, x.device)
+    _check(lib().pti_test_q8_gemv_stall(_ptr(w), rows, cols, n, _ptr(x), _ptr(y), _ptr(ws),
+                                        0 if ws is None else ws.numel() * ws.element_size(), _stream(stream),
+                                        int(stall_unit), int(wait_ns)), "pti_test_q8_gemv_stall")
+    return y
 
 
 def device_error() -> int:

@@ -62,16 +62,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false if it
-// has not completed within kWaitTimeoutNs (or 2^30 polls), or, when
+// has not completed within `timeout_ns` (or 2^30 polls), or, when
 // `abort_flag` is a shared-memory address other than 0, as soon as the 32-bit
 // word there becomes non-zero (another warp of the CTA recorded an error).
-static __device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t abort_flag) {
+static __device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t abort_flag,
+                                                      uint64_t timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1; i < (1u << 30); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) return false;
       if (abort_flag != 0) {
         uint32_t f;
         asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(f) : "r"(abort_flag) : "memory");

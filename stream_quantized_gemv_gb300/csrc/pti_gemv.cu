@@ -14,14 +14,18 @@ namespace pti {
 namespace {
 
 // ---------------------------------------------------------------------------
-// Plain per-row kernels for shapes outside the fast path: one warp per row,
+// Plain per-row kernel for shapes outside the fast path: one warp per row,
 // lanes stride over the blocks, each block's products summed into a fresh
-// partial and scaled once.
+// partial that is scaled once.  The block layout is a parameter: a block of
+// kBlock bytes holds its binary16 scale at byte kScale and the int8 of column
+// i at byte kQ + kStride * i.  Q8 is (34, 0, 2, 1); a twin block is read as
+// model A (68, 0, 5, 2), whose bytes are the upper halves of the payload's
+// little-endian 16-bit elements, and as model B (68, 2, 4, 2), the lower
+// halves.
 // ---------------------------------------------------------------------------
-template <int N>
-__global__ void __launch_bounds__(256) q8_rowwise_kernel(const uint8_t *__restrict__ w, int64_t rows,
-                                                         int64_t cols, const float *__restrict__ x,
-                                                         float *__restrict__ y) {
+template <int N, int kBlock, int kScale, int kQ, int kStride>
+__global__ void __launch_bounds__(256) rowwise_kernel(const uint8_t *__restrict__ w, int64_t rows, int64_t cols,
+                                                      const float *__restrict__ x, float *__restrict__ y) {
   const int lane = threadIdx.x & 31;
   const int64_t nb = cols / 32;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -30,15 +34,16 @@ __global__ void __launch_bounds__(256) q8_rowwise_kernel(const uint8_t *__restri
 #pragma unroll
     for (int s = 0; s < N; ++s) acc[s] = 0.0f;
     for (int64_t b = lane; b < nb; b += 32) {
-      const uint8_t *blk = w + (row * nb + b) * 34;
-      const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
+      const uint8_t *blk = w + (row * nb + b) * kBlock;
+      const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk + kScale));
+      const float *xb = x + 32 * b;
       float part[N];
 #pragma unroll
       for (int s = 0; s < N; ++s) part[s] = 0.0f;
       for (int i = 0; i < 32; ++i) {
-        const float q = static_cast<float>(static_cast<int8_t>(blk[2 + i]));
+        const float q = static_cast<float>(static_cast<int8_t>(blk[kQ + kStride * i]));
 #pragma unroll
-        for (int s = 0; s < N; ++s) part[s] = fmaf(q, x[s * cols + 32 * b + i], part[s]);
+        for (int s = 0; s < N; ++s) part[s] = fmaf(q, xb[s * cols + i], part[s]);
       }
 #pragma unroll
       for (int s = 0; s < N; ++s) acc[s] = fmaf(d, part[s], acc[s]);
@@ -52,50 +57,21 @@ __global__ void __launch_bounds__(256) q8_rowwise_kernel(const uint8_t *__restri
   }
 }
 
-__global__ void __launch_bounds__(256) twin_rowwise_kernel(const uint8_t *__restrict__ w, int64_t rows,
-                                                           int64_t cols, const float *__restrict__ xa,
-                                                           const float *__restrict__ xb,
-                                                           float *__restrict__ ya, float *__restrict__ yb) {
-  const int lane = threadIdx.x & 31;
-  const int64_t nb = cols / 32;
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; row < rows; row += warps) {
-    float acc_a = 0.0f, acc_b = 0.0f;
-    for (int64_t b = lane; b < nb; b += 32) {
-      const uint8_t *blk = w + (row * nb + b) * 68;
-      const float da = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
-      const float db = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk + 2));
-      float pa = 0.0f, pb = 0.0f;
-      for (int i = 0; i < 32; ++i) {
-        const uint16_t pw = *reinterpret_cast<const uint16_t *>(blk + 4 + 2 * i);
-        const float qa = static_cast<float>(static_cast<int8_t>(pw >> 8));
-        const float qb = static_cast<float>(static_cast<int8_t>(pw & 0xFF));
-        pa = fmaf(qa, xa[32 * b + i], pa);
-        pb = fmaf(qb, xb[32 * b + i], pb);
-      }
-      acc_a = fmaf(da, pa, acc_a);
-      acc_b = fmaf(db, pb, acc_b);
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-      acc_a += __shfl_xor_sync(0xFFFFFFFFu, acc_a, o);
-      acc_b += __shfl_xor_sync(0xFFFFFFFFu, acc_b, o);
-    }
-    if (lane == 0) {
-      ya[row] = acc_a;
-      yb[row] = acc_b;
-    }
-  }
+template <int N, int kBlock, int kScale, int kQ, int kStride>
+pti_status launch_rowwise(const void *w, int64_t rows, int64_t cols, const float *x, float *y,
+                          cudaStream_t stream) {
+  const int sms = current_device_sms();
+  if (sms <= 0) return PTI_ERR_CUDA;
+  const int64_t blocks = std::min<int64_t>((rows + 7) / 8, static_cast<int64_t>(sms) * 16);
+  rowwise_kernel<N, kBlock, kScale, kQ, kStride><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const uint8_t *>(w), rows, cols, x, y);
+  return launch_status();
 }
 
 template <int N>
 pti_status launch_q8_rowwise(const void *w, int64_t rows, int64_t cols, const float *x, float *y,
                              cudaStream_t stream) {
-  const int sms = current_device_sms();
-  if (sms <= 0) return PTI_ERR_CUDA;
-  const int64_t blocks = std::min<int64_t>((rows + 7) / 8, static_cast<int64_t>(sms) * 16);
-  q8_rowwise_kernel<N><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(static_cast<const uint8_t *>(w), rows,
-                                                                          cols, x, y);
-  return launch_status();
+  return launch_rowwise<N, 34, 0, 2, 1>(w, rows, cols, x, y, stream);
 }
 
 }  // namespace
@@ -209,16 +185,12 @@ pti_status twin_gemv(const void *w_twin, int64_t rows, int64_t cols, int n, cons
       return launch_fast<Fmt::Twin, 2>(w_twin, rows, cols, x_a, x_b, y_a, y_b, workspace, st, pdl);
     }
   }
-  const int sms = current_device_sms();
-  if (sms <= 0) return PTI_ERR_CUDA;
-  const int64_t blocks = std::min<int64_t>((rows + 7) / 8, static_cast<int64_t>(sms) * 16);
-  for (int s = 0; s < n; ++s) {
-    twin_rowwise_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        static_cast<const uint8_t *>(w_twin), rows, cols, x_a + static_cast<int64_t>(s) * cols,
-        x_b + static_cast<int64_t>(s) * cols, y_a + static_cast<int64_t>(s) * rows, y_b + static_cast<int64_t>(s) * rows);
-    if (const pti_status e = launch_status(); e != PTI_OK) return e;
-  }
-  return PTI_OK;
+  // the plain kernel, once per model (model A: upper bytes, model B: lower)
+  const pti_status e = n == 1 ? launch_rowwise<1, 68, 0, 5, 2>(w_twin, rows, cols, x_a, y_a, st)
+                              : launch_rowwise<2, 68, 0, 5, 2>(w_twin, rows, cols, x_a, y_a, st);
+  if (e != PTI_OK) return e;
+  return n == 1 ? launch_rowwise<1, 68, 2, 4, 2>(w_twin, rows, cols, x_b, y_b, st)
+                : launch_rowwise<2, 68, 2, 4, 2>(w_twin, rows, cols, x_b, y_b, st);
 }
 
 }  // namespace
@@ -305,6 +277,39 @@ extern "C" pti_status pti_q8_gemv_nstream_noalloc(const void *w_q8, int64_t rows
   }
   return pti_q8_gemv_nstream(w_q8, rows, cols, n_streams, x, y, scratch, need > 0 ? kNoAllocScratchBytes : 0,
                              stream);
+}
+
+// Testing hook: the fast-path Q8 GEMV with a stalled copy (see pti.h).
+extern "C" pti_status pti_test_q8_gemv_stall(const void *w_q8, int64_t rows, int64_t cols, int n_streams,
+                                             const float *x, float *y, void *workspace, size_t workspace_bytes,
+                                             pti_stream_t stream, int64_t stall_unit, uint64_t wait_ns) {
+  if (w_q8 == nullptr || x == nullptr || y == nullptr || workspace == nullptr) return PTI_ERR_NULL;
+  if (const pti_status st = check_gemv_shape(rows, cols); st != PTI_OK) return st;
+  if (cols % 256 != 0) return PTI_ERR_SHAPE;
+  if (n_streams < 1 || n_streams > 4) return PTI_ERR_NSTREAMS;
+  if (!aligned(w_q8, 16) || !aligned(x, 16) || !aligned(y, 4) || !aligned(workspace, 256)) return PTI_ERR_ALIGN;
+  if (workspace_bytes < fast_workspace_bytes(n_streams)) return PTI_ERR_WORKSPACE;
+  if (wait_ns < 1000 || wait_ns > kWaitTimeoutNs) return PTI_ERR_VALUE;
+  const int sms = current_device_sms();
+  if (sms <= 0) return PTI_ERR_CUDA;
+  const TilePlan p = plan_tiles<Fmt::Q8, 1, Epi::Plain>(rows, cols, sms);
+  const int64_t cta0_units = p.units / p.grid;
+  if (stall_unit < kMaxStages || stall_unit >= cta0_units) return PTI_ERR_VALUE;
+  // (the grid and the unit split do not depend on the stream count)
+  const uint64_t w_bytes = static_cast<uint64_t>(rows) * (cols / 32) * 34;
+  const uint64_t y_bytes = static_cast<uint64_t>(n_streams) * rows * 4;
+  const uint64_t x_bytes = static_cast<uint64_t>(n_streams) * cols * 4;
+  const size_t need = fast_workspace_bytes(n_streams);
+  if (overlaps(y, y_bytes, w_q8, w_bytes) || overlaps(y, y_bytes, x, x_bytes) || overlaps(workspace, need, y, y_bytes) ||
+      overlaps(workspace, need, w_q8, w_bytes) || overlaps(workspace, need, x, x_bytes))
+    return PTI_ERR_ALIAS;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (n_streams) {
+    case 1: return launch_fast<Fmt::Q8, 1>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, s, false, wait_ns, stall_unit);
+    case 2: return launch_fast<Fmt::Q8, 2>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, s, false, wait_ns, stall_unit);
+    case 3: return launch_fast<Fmt::Q8, 3>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, s, false, wait_ns, stall_unit);
+    default: return launch_fast<Fmt::Q8, 4>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, s, false, wait_ns, stall_unit);
+  }
 }
 
 extern "C" pti_status pti_device_error(uint32_t *code_out) {

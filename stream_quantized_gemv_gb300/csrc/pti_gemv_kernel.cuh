@@ -19,29 +19,28 @@
 //    [c U / G, (c+1) U / G) in row-major order, so every SM streams the same
 //    number of bytes.  Row tiles shared by several CTAs are combined by a
 //    small kernel launched right behind the GEMV (partials in a
-//    caller-supplied workspace, summed in a fixed CTA order); the persistent
-//    decode kernel instead lets the last CTA to finish a tile combine it (an
-//    atomic ticket per tile).
-//  * Lane 0 of consumer warp 0 issues the copies into a ring of up to 6 stages
-//    guarded by mbarriers (it refills a slot once every warp has released
-//    it); 16 warps compute.  Q8: warp w always computes block w % 8 of each
-//    unit for 64 rows (two per lane), reading each row's 40-byte window around
+//    caller-supplied workspace, summed in a fixed CTA order).
+//  * Lane 0 of the producer warp issues the copies into a ring of up to 6
+//    stages guarded by mbarriers (it refills a slot once every consumer warp
+//    has released it).
+//  * Q8 (16 consumer warps): warp w always computes block w % 8 of each unit
+//    for 64 rows (two per lane), reading each row's 40-byte window around
 //    the block with five aligned 8-byte loads; the four warps of a scheduler
-//    share one code body.  Twin: warp w computes half of block w % 4 (16
+//    share one code body.
+//  * Twin (16 consumer warps): warp w computes half of block w % 4 (16
 //    columns of both models) of each unit for 64 rows, two per lane; the
 //    block is fixed per scheduler, so its byte offsets are compile-time.
 //  * Each stage also holds the unit's slice of the activations (N x 1 KB,
 //    stream-major), fetched by one bulk copy per stream next to the weight
-//    tile.  Every warp reads them with broadcast loads and reuses them for its
-//    64 rows, so activation traffic is one slice per unit and does not grow
+//    tile, so activation traffic is one slice per unit and does not grow
 //    with the number of rows (the L2 thrash the pages diagnose for the
 //    per-row-block design comes from re-reading x once per row block).
 //  * Dequantisation is exact (see pti_device.cuh); products use packed
-//    f32x2 FMAs.  A warp's products of one unit are summed into a fresh
-//    partial (16 Q8 or 8 twin products per half of the pair), which is then
-//    added to the running accumulator once per super-block, so an output's
-//    longest chain of dependent roundings is about K/256 (Q8) or K/128 (twin)
-//    plus a few dozen.
+//    f32x2 FMAs.  A lane's products of one block and unit are summed into a
+//    fresh partial (16 Q8 or 8 twin products per half of the f32x2 pair),
+//    which is then added to the running accumulator once per unit, so an
+//    output's longest chain of dependent roundings is about K/256 (Q8) or
+//    K/128 (twin) plus a few dozen.
 //  * Programmatic dependent launch: the producer fetches its first weight
 //    tiles before waiting for the previous kernel in the stream, and only then
 //    fetches activations; nothing is written before that wait.
@@ -73,11 +72,11 @@ namespace {
 constexpr int kSBBytes = 272;                          // super-block bytes (17 chunks of 16)
 constexpr int kRowsPerTile = 128;                      // rows per unit
 constexpr int kMaxStages = 6;
-constexpr int kWarpCount = 16;  // consumer warps, 4 per scheduler
 constexpr int kStageBytes = kRowsPerTile * kSBBytes;   // 34816
 constexpr int kMaxGrid = 320;
 constexpr int kSmemOptin = 232448;                     // 227 KB per CTA
 constexpr uint32_t kBarConsumers = 1;                  // named barrier of the consumer warps
+constexpr int kRedWarps = 8;                           // warps whose sums make up one output element
 
 __device__ unsigned int g_device_error = 0;
 
@@ -96,7 +95,7 @@ struct Traits;
 template <int N>
 struct Traits<Fmt::Q8, N> {
   static constexpr int kOut = N;                   // output vectors
-  static constexpr int kWarps = kWarpCount;
+  static constexpr int kWarps = 16;                // four per scheduler
   static constexpr int kColsPerSB = 256;
   static constexpr int kXStreams = N;
   static constexpr int kBlockBytes = 34;
@@ -105,20 +104,21 @@ struct Traits<Fmt::Q8, N> {
 template <int N>
 struct Traits<Fmt::Twin, N> {
   static constexpr int kOut = 2 * N;
-  static constexpr int kWarps = kWarpCount;
+  static constexpr int kWarps = 16;                // four per scheduler
   static constexpr int kColsPerSB = 128;
   static constexpr int kXStreams = 2 * N;
   static constexpr int kBlockBytes = 68;
 };
 
 // One pipeline stage: the 128 x 272-byte weight tile followed by the unit's
-// activations, stream-major (kXStreams rows of kColsPerSB floats).
+// activations, stream-major (kXStreams rows of kColsPerSB floats).  kRedBytes:
+// the parked sums of two row tiles, kRedWarps per output element.
 template <Fmt F, int N>
 struct Stage {
   static constexpr int kXStreamBytes = Traits<F, N>::kColsPerSB * 4;
   static constexpr int kXBytes = Traits<F, N>::kXStreams * kXStreamBytes;
   static constexpr int kBytes = ((kStageBytes + kXBytes) + 1023) / 1024 * 1024;
-  static constexpr int kRedBytes = 2 * Traits<F, N>::kWarps * Traits<F, N>::kOut * 64 * 4;
+  static constexpr int kRedBytes = 2 * kRedWarps * Traits<F, N>::kOut * kRowsPerTile * 4;
 };
 
 struct GemvArgs {
@@ -127,7 +127,6 @@ struct GemvArgs {
   float *y0;        // Q8: y [N][rows]; twin: y_a [N][rows]
   float *y1;        // twin: y_b [N][rows]
   float *part;      // workspace: [grid][2 slots][kOut][128] partial sums
-  unsigned int *tickets;  // in-kernel combining only: [n_rb] arrival counters, zero at start
   int64_t rows, cols, units;  // GateUp: rows = gate rows = up rows = outputs per stream
   int32_t n_sb, n_rb, grid, stages;
   // Fused epilogues only (Epi::GateUp, Epi::Down):
@@ -136,155 +135,234 @@ struct GemvArgs {
   double inv_len_in;   // 1 / length of each input vector
   double eps;          // added to the mean square before the square root
   int32_t n_sq_in;
-  int32_t combine_in_kernel;  // 1: tickets and the last CTA combine shared tiles; 0: combine_tiles_kernel does
   // Fused epilogues of the chained pass: the input scales the GEMV derived, for
   // its tile-combine kernel ([kOut] floats, written by CTA 0).
   float *scale_out;
   int32_t prefetch_all;  // 1: fetch every initial stage's weights before waiting for the previous kernel
+  // Pipeline waits give up after this many ns (0: kWaitTimeoutNs).
+  uint64_t wait_ns = 0;
+  // Testing only: the producer of CTA 0 issues no copy from its unit
+  // `stall_unit` on (-1: never; must be at least the ring depth), as if the
+  // copy never arrived; the consumers' wait for it then runs out after
+  // wait_ns.
+  int64_t stall_unit = -1;
 };
 
-// Rows handled by one consumer warp: lane l owns rows 64h + l and 64h + 32 + l
-// of the tile (h = the warp's half).  (Four rows per lane halves the
-// activation loads per weight but needs 8 instead of 16 warps per tile within
-// the register budget; measured slower.)
-constexpr int kTaskSlots = 2;
-
-// One Q8 block b of the super-block (columns 32b .. 32b+31) for the lane's
-// two rows of half h.  The block's 34 bytes start at byte 34b = 32b + 2b of
-// the row.  With b = 2c + e, the 40-byte window that starts at byte
-// 32b + 8 (c >= 2) of the row (five aligned 8-byte loads; b is fixed per warp,
-// so the offset is loop-invariant) holds the block from word c % 2 on, at
-// half-word e: the scale is half-word e of that word, weight pair j (columns
-// 32b+2j, 32b+2j+1) is at byte 2e+2+2j.  The warps of a scheduler share
-// c % 2 and e, so they run one code body.  (Five 8-byte loads replace three
-// 16-byte loads and ten selects: measured 5% faster at N = 4, 7% at N = 1.)
-template <int N, int E, int CLO>
-__device__ __forceinline__ void q8_block_body(const uint8_t *tile, const uint8_t *xblk, uint32_t lane, uint32_t half,
-                                              uint32_t win_off, bool c_hi, uint64_t (&acc)[kTaskSlots][N]) {
-  uint32_t w[kTaskSlots][9];
-  ScalePair sc[kTaskSlots];
-#pragma unroll
-  for (int r = 0; r < kTaskSlots; ++r) {
-    const uint8_t *win = tile + (half * 64 + r * 32 + lane) * kSBBytes + win_off + (c_hi ? 8u : 0u);
-    uint32_t t1[10];
-#pragma unroll
-    for (int k = 0; k < 5; ++k) {
-      const uint2 v = *reinterpret_cast<const uint2 *>(win + 8 * k);
-      t1[2 * k] = v.x;
-      t1[2 * k + 1] = v.y;
-    }
-#pragma unroll
-    for (int k = 0; k < 9; ++k) w[r][k] = t1[k + CLO];
-    sc[r] = make_scale(E ? (w[r][0] >> 16) : (w[r][0] & 0xFFFFu));
-#pragma unroll
-    for (int k = 0; k < 9; ++k) w[r][k] ^= 0x80808080u;
-  }
-  uint64_t p[kTaskSlots][N];
-  static_for<0, 8>([&](auto jc) {  // two weight pairs per step: one 16-byte x load per stream
-    constexpr int j0 = 2 * decltype(jc)::value;
-    ulonglong2 xv[N];
-#pragma unroll
-    for (int st = 0; st < N; ++st)
-      xv[st] = *reinterpret_cast<const ulonglong2 *>(xblk + st * Stage<Fmt::Q8, N>::kXStreamBytes + j0 * 8);
-    static_for<0, 2>([&](auto jj_) {
-      constexpr int j = j0 + decltype(jj_)::value;
-      constexpr int t = 2 * E + 2 + 2 * j;  // byte of the pair's first weight in the aligned words
-#pragma unroll
-      for (int r = 0; r < kTaskSlots; ++r) {
-        const uint64_t wq = dequant2(w[r][t / 4], t % 4, w[r][t / 4], t % 4 + 1, sc[r]);
-        static_for<0, N>([&](auto sc_) {
-          constexpr int st = decltype(sc_)::value;
-          const uint64_t xs = (j & 1) ? xv[st].y : xv[st].x;
-          if constexpr (j == 0) p[r][st] = fmul2(wq, xs);
-          else p[r][st] = ffma2(wq, xs, p[r][st]);
-        });
-      }
-    });
-  });
-#pragma unroll
-  for (int r = 0; r < kTaskSlots; ++r)
-    static_for<0, N>([&](auto sc_) {
-      constexpr int st = decltype(sc_)::value;
-      acc[r][st] = fadd2(acc[r][st], p[r][st]);
-    });
+__device__ __forceinline__ uint64_t wait_limit(const GemvArgs &a) {
+  return a.wait_ns != 0 ? a.wait_ns : kWaitTimeoutNs;
 }
 
-// One twin block b of the super-block (columns 32b .. 32b+31, bytes
-// 68b .. 68b+67 of each row) for the lane's two rows of half h, columns
-// 16ch .. 16ch+15 of the block.  The block's scale word (binary16 scale of A,
-// then of B) is at byte 68b; payload word k (columns 2k, 2k+1) at
-// 68b + 4 + 4k holds the bytes [B(2k), A(2k), B(2k+1), A(2k+1)] (each uint16
-// is A << 8 | B, stored little-endian).  The warp's eight payload words start
-// (68b + 4) % 16 bytes past a 16-byte boundary: two or three aligned 16-byte
-// loads, with b (= the warp's scheduler) a compile-time constant, plus one
-// 4-byte load of the scales.
-template <int N, int B>
-__device__ __forceinline__ void twin_block_body(const uint8_t *tile, const uint8_t *xsb, uint32_t lane,
-                                                uint32_t half, uint32_t ch, uint64_t (&acc)[kTaskSlots][2 * N]) {
-  constexpr int kP = (68 * B + 4) % 16;         // payload offset past the 16-byte boundary
-  constexpr int kChunks = (kP + 32 + 15) / 16;  // 16-byte loads covering the 32 payload bytes
-  constexpr int kXS = Stage<Fmt::Twin, N>::kXStreamBytes;
-  uint32_t w[kTaskSlots][8];
-  ScalePair sa[kTaskSlots], sb[kTaskSlots];
-#pragma unroll
-  for (int r = 0; r < kTaskSlots; ++r) {
-    const uint8_t *row = tile + (half * 64 + r * 32 + lane) * kSBBytes;
-    const uint32_t scales = *reinterpret_cast<const uint32_t *>(row + 68 * B);
-    const uint8_t *pl = row + (68 * B + 4 - kP) + 32 * ch;
-    uint32_t words[4 * kChunks];
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-      const uint4 v = *reinterpret_cast<const uint4 *>(pl + 16 * c);
-      words[4 * c] = v.x;
-      words[4 * c + 1] = v.y;
-      words[4 * c + 2] = v.z;
-      words[4 * c + 3] = v.w;
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) w[r][k] = words[kP / 4 + k] ^ 0x80808080u;
-    sa[r] = make_scale(scales & 0xFFFFu);
-    sb[r] = make_scale(scales >> 16);
+// ---------------------------------------------------------------------------
+// Q8 consumer (16 warps).  Warp w computes block B = w % 8 of every unit
+// (columns 32B .. 32B+31, the block's 34 bytes at row byte 34B = 32B + 2B)
+// for the 64 rows of half hf = w / 8, two rows per lane (64 hf + l and
+// 64 hf + 32 + l).  With B = 2c + e, the 40-byte window that starts at byte
+// 32B + 8 [c >= 2] of the row (five aligned 8-byte loads; B is fixed per
+// warp, so the offset is loop-invariant) holds the block from word c % 2 on,
+// at half-word e: the scale is half-word e of that word, weight pair j
+// (columns 32B+2j, 32B+2j+1) is at byte 2e+2+2j.  The warps of a scheduler
+// (w % 4) share c % 2 and e (template parameters E and CLO), so they run one
+// code body.  (Five 8-byte loads replace three 16-byte loads and ten selects:
+// measured 5% faster at N = 4, 7% at N = 1.)
+//
+// Activations are warp-broadcast 16-byte loads (two weight pairs of one
+// stream) reused across the lane's two rows; each weight pair is dequantised
+// to q d exactly (dequant2) and its products with the N activation pairs go
+// to a fresh partial (16 dependent FMAs per half of the pair), which is added
+// to the row's accumulator once per unit.
+// ---------------------------------------------------------------------------
+template <int N, int E, int CLO>
+struct Q8Pair {
+  static constexpr int kSlots = 2;
+  uint64_t acc[kSlots][N];
+  uint32_t lane, half, blk;
+
+  __device__ __forceinline__ void init(uint32_t warp, uint32_t lane_) {
+    lane = lane_;
+    half = warp >> 3;
+    blk = warp & 7u;
   }
-  const uint8_t *xcol = xsb + (32 * B) * 4 + ch * 64;  // column 32b + 16ch of stream 0
-  uint64_t pa[kTaskSlots][N], pb[kTaskSlots][N];
-  static_for<0, 4>([&](auto jc) {  // two payload words (four columns) per step
-    constexpr int k0 = 2 * decltype(jc)::value;
-    ulonglong2 xa[N], xb[N];
+
+  __device__ __forceinline__ void reset() {
 #pragma unroll
-    for (int s = 0; s < N; ++s) {
-      xa[s] = *reinterpret_cast<const ulonglong2 *>(xcol + s * kXS + k0 * 8);
-      xb[s] = *reinterpret_cast<const ulonglong2 *>(xcol + (N + s) * kXS + k0 * 8);
+    for (int r = 0; r < kSlots; ++r)
+#pragma unroll
+      for (int s = 0; s < N; ++s) acc[r][s] = 0ull;
+  }
+
+  template <int kXS>
+  __device__ __forceinline__ void unit(const uint8_t *tile, const uint8_t *xsb) {
+    const uint8_t *xblk = xsb + 128u * blk;  // block B's 32 activations of stream 0
+    const uint32_t win_off = 32u * blk + ((blk & 4u) != 0u ? 8u : 0u);
+    uint32_t w[kSlots][9];
+    ScalePair sc[kSlots];
+#pragma unroll
+    for (int r = 0; r < kSlots; ++r) {
+      const uint8_t *win = tile + (half * 64 + r * 32 + lane) * kSBBytes + win_off;
+      uint32_t t1[10];
+#pragma unroll
+      for (int k = 0; k < 5; ++k) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(win + 8 * k);
+        t1[2 * k] = v.x;
+        t1[2 * k + 1] = v.y;
+      }
+#pragma unroll
+      for (int k = 0; k < 9; ++k) w[r][k] = t1[k + CLO];
+      sc[r] = make_scale(E ? (w[r][0] >> 16) : (w[r][0] & 0xFFFFu));
+#pragma unroll
+      for (int k = 0; k < 9; ++k) w[r][k] ^= 0x80808080u;
     }
-    static_for<0, 2>([&](auto kk_) {
-      constexpr int kk = decltype(kk_)::value;
-      constexpr int k = k0 + kk;
+    uint64_t p[kSlots][N];
+    static_for<0, 8>([&](auto jc) {  // two weight pairs per step: one 16-byte x load per stream
+      constexpr int j0 = 2 * decltype(jc)::value;
+      ulonglong2 xv[N];
 #pragma unroll
-      for (int r = 0; r < kTaskSlots; ++r) {
-        const uint64_t wa = dequant2(w[r][k], 1, w[r][k], 3, sa[r]);
-        const uint64_t wb = dequant2(w[r][k], 0, w[r][k], 2, sb[r]);
+      for (int st = 0; st < N; ++st) xv[st] = *reinterpret_cast<const ulonglong2 *>(xblk + st * kXS + j0 * 8);
+      static_for<0, 2>([&](auto jj_) {
+        constexpr int j = j0 + decltype(jj_)::value;
+        constexpr int t = 2 * E + 2 + 2 * j;  // byte of the pair's first weight in the aligned words
 #pragma unroll
-        for (int s = 0; s < N; ++s) {
-          const uint64_t x_a = kk ? xa[s].y : xa[s].x;
-          const uint64_t x_b = kk ? xb[s].y : xb[s].x;
-          if constexpr (k == 0) {
-            pa[r][s] = fmul2(wa, x_a);
-            pb[r][s] = fmul2(wb, x_b);
-          } else {
-            pa[r][s] = ffma2(wa, x_a, pa[r][s]);
-            pb[r][s] = ffma2(wb, x_b, pb[r][s]);
+        for (int r = 0; r < kSlots; ++r) {
+          const uint64_t wq = dequant2(w[r][t / 4], t % 4, w[r][t / 4], t % 4 + 1, sc[r]);
+#pragma unroll
+          for (int st = 0; st < N; ++st) {
+            const uint64_t xs = (j & 1) ? xv[st].y : xv[st].x;
+            if constexpr (j == 0) p[r][st] = fmul2(wq, xs);
+            else p[r][st] = ffma2(wq, xs, p[r][st]);
           }
         }
-      }
+      });
     });
-  });
 #pragma unroll
-  for (int r = 0; r < kTaskSlots; ++r)
+    for (int r = 0; r < kSlots; ++r)
 #pragma unroll
-    for (int s = 0; s < N; ++s) {
-      acc[r][s] = fadd2(acc[r][s], pa[r][s]);
-      acc[r][N + s] = fadd2(acc[r][N + s], pb[r][s]);
+      for (int st = 0; st < N; ++st) acc[r][st] = fadd2(acc[r][st], p[r][st]);
+  }
+
+  // End of a row tile: red[sl][warp][s][row of the half] (64 rows per warp).
+  template <int kOut>
+  __device__ __forceinline__ void park(float *red, int sl, uint32_t warp) const {
+#pragma unroll
+    for (int r = 0; r < kSlots; ++r)
+#pragma unroll
+      for (int s = 0; s < kOut; ++s) {
+        const float2 v = unpack2(acc[r][s]);
+        red[((sl * 16 + static_cast<int>(warp)) * kOut + s) * 64 + r * 32 + static_cast<int>(lane)] = v.x + v.y;
+      }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Twin consumer.  Warp w computes columns 16ch .. 16ch+15 (ch = w / 8) of
+// block B = w % 4 of the super-block, both models, for the 64 rows of half
+// hf = (w / 4) % 2, two rows per lane (64 hf + l and 64 hf + 32 + l).  The
+// block's scale word (binary16 scale of A, then of B) is at byte 68B; payload
+// word k (columns 2k, 2k+1) at 68B + 4 + 4k holds the bytes
+// [B(2k), A(2k), B(2k+1), A(2k+1)] (each uint16 is A << 8 | B, stored
+// little-endian).  The warp's eight payload words start (68B + 4) % 16 bytes
+// past a 16-byte boundary: two or three aligned 16-byte loads, with B (= the
+// warp's scheduler) a compile-time constant, plus one 4-byte load of the
+// scales.  Products go to fresh partials per unit (8 dependent FMAs per half
+// of the pair), added to the accumulators once per unit.
+// ---------------------------------------------------------------------------
+template <int N, int B>
+struct TwinSlab {
+  static constexpr int kSlots = 2;
+  uint64_t acc[kSlots][2 * N];
+  uint32_t lane, half, ch;
+
+  __device__ __forceinline__ void init(uint32_t warp, uint32_t lane_) {
+    lane = lane_;
+    half = (warp >> 2) & 1u;
+    ch = warp >> 3;
+  }
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int r = 0; r < kSlots; ++r)
+#pragma unroll
+      for (int s = 0; s < 2 * N; ++s) acc[r][s] = 0ull;
+  }
+
+  template <int kXS>
+  __device__ __forceinline__ void unit(const uint8_t *tile, const uint8_t *xsb) {
+    constexpr int kP = (68 * B + 4) % 16;         // payload offset past the 16-byte boundary
+    constexpr int kChunks = (kP + 32 + 15) / 16;  // 16-byte loads covering the 32 payload bytes
+    uint32_t w[kSlots][8];
+    ScalePair sa[kSlots], sb[kSlots];
+#pragma unroll
+    for (int r = 0; r < kSlots; ++r) {
+      const uint8_t *row = tile + (half * 64 + r * 32 + lane) * kSBBytes;
+      const uint32_t scales = *reinterpret_cast<const uint32_t *>(row + 68 * B);
+      const uint8_t *pl = row + (68 * B + 4 - kP) + 32 * ch;
+      uint32_t words[4 * kChunks];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(pl + 16 * c);
+        words[4 * c] = v.x;
+        words[4 * c + 1] = v.y;
+        words[4 * c + 2] = v.z;
+        words[4 * c + 3] = v.w;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) w[r][k] = words[kP / 4 + k] ^ 0x80808080u;
+      sa[r] = make_scale(scales & 0xFFFFu);
+      sb[r] = make_scale(scales >> 16);
     }
-}
+    const uint8_t *xcol = xsb + (32 * B) * 4 + ch * 64;  // column 32B + 16ch of stream 0
+    uint64_t pa[kSlots][N], pb[kSlots][N];
+    static_for<0, 4>([&](auto jc) {  // two payload words (four columns) per step
+      constexpr int k0 = 2 * decltype(jc)::value;
+      ulonglong2 xa[N], xb[N];
+#pragma unroll
+      for (int s = 0; s < N; ++s) {
+        xa[s] = *reinterpret_cast<const ulonglong2 *>(xcol + s * kXS + k0 * 8);
+        xb[s] = *reinterpret_cast<const ulonglong2 *>(xcol + (N + s) * kXS + k0 * 8);
+      }
+      static_for<0, 2>([&](auto kk_) {
+        constexpr int kk = decltype(kk_)::value;
+        constexpr int k = k0 + kk;
+#pragma unroll
+        for (int r = 0; r < kSlots; ++r) {
+          // bytes 1 and 3 of a payload word are model A's weights, 0 and 2 model B's
+          const uint64_t wa = dequant2(w[r][k], 1, w[r][k], 3, sa[r]);
+          const uint64_t wb = dequant2(w[r][k], 0, w[r][k], 2, sb[r]);
+#pragma unroll
+          for (int s = 0; s < N; ++s) {
+            const uint64_t x_a = kk ? xa[s].y : xa[s].x;
+            const uint64_t x_b = kk ? xb[s].y : xb[s].x;
+            if constexpr (k == 0) {
+              pa[r][s] = fmul2(wa, x_a);
+              pb[r][s] = fmul2(wb, x_b);
+            } else {
+              pa[r][s] = ffma2(wa, x_a, pa[r][s]);
+              pb[r][s] = ffma2(wb, x_b, pb[r][s]);
+            }
+          }
+        }
+      });
+    });
+#pragma unroll
+    for (int r = 0; r < kSlots; ++r)
+#pragma unroll
+      for (int s = 0; s < N; ++s) {
+        acc[r][s] = fadd2(acc[r][s], pa[r][s]);
+        acc[r][N + s] = fadd2(acc[r][N + s], pb[r][s]);
+      }
+  }
+
+  // End of a row tile: red[sl][warp][s][row of the half] (64 rows per warp).
+  template <int kOut>
+  __device__ __forceinline__ void park(float *red, int sl, uint32_t warp) const {
+#pragma unroll
+    for (int r = 0; r < kSlots; ++r)
+#pragma unroll
+      for (int s = 0; s < kOut; ++s) {
+        const float2 v = unpack2(acc[r][s]);
+        red[((sl * 16 + static_cast<int>(warp)) * kOut + s) * 64 + r * 32 + static_cast<int>(lane)] = v.x + v.y;
+      }
+  }
+};
 
 __device__ __forceinline__ int32_t cta_of_unit(int64_t u, int64_t units, int32_t grid) {
   return static_cast<int32_t>(((u + 1) * grid - 1) / units);
@@ -426,23 +504,28 @@ __device__ __forceinline__ void gateup_epilogue(const GemvArgs &a, const float *
 }
 
 // Decode-pass epilogue of down tile rb: x' = a (W h) with a the RMS scale of
-// h; writes x' [kOut][rows] and the tile's sum of x'^2 per vector.
+// h; writes x' [kOut][rows] and the tile's sum of x'^2 per vector.  Element
+// e = (s, r) = (e / 128, e % 128) is handled by thread e % threads; the sums
+// of squares are formed per group of 32 elements (a warp's share) and then
+// over the 4 groups of a vector, in the same order for any thread count.
 template <int kOut>
 __device__ __forceinline__ void down_epilogue(const GemvArgs &a, const float *tile_out, const float *scale,
                                               float *wsum, int32_t rb, uint32_t tid, uint32_t consumer_threads) {
-  float v = 0.0f;
-  if (tid < static_cast<uint32_t>(kOut * kRowsPerTile)) {
-    const int s = static_cast<int>(tid >> 7), r = static_cast<int>(tid & 127u);
-    const int64_t row = static_cast<int64_t>(rb) * kRowsPerTile + r;
-    if (row < a.rows) {
-      v = tile_out[s * kRowsPerTile + r] * scale[s];
-      a.y0[s * a.rows + row] = v;
+  for (uint32_t e0 = 0; e0 < static_cast<uint32_t>(kOut * kRowsPerTile); e0 += consumer_threads) {
+    const uint32_t e = e0 + tid;
+    float v = 0.0f;
+    if (e < static_cast<uint32_t>(kOut * kRowsPerTile)) {
+      const int s = static_cast<int>(e >> 7), r = static_cast<int>(e & 127u);
+      const int64_t row = static_cast<int64_t>(rb) * kRowsPerTile + r;
+      if (row < a.rows) {
+        v = tile_out[s * kRowsPerTile + r] * scale[s];
+        a.y0[s * a.rows + row] = v;
+      }
     }
-  }
-  const uint32_t warp = tid >> 5;
-  if (warp < static_cast<uint32_t>(4 * kOut)) {
-    const float q = warp_sum(v * v);
-    if ((tid & 31u) == 0) wsum[warp] = q;
+    if ((e0 >> 5) + (tid >> 5) < static_cast<uint32_t>(4 * kOut)) {
+      const float q = warp_sum(v * v);
+      if ((tid & 31u) == 0) wsum[e >> 5] = q;
+    }
   }
   named_barrier(kBarConsumers, consumer_threads);
   if (tid < static_cast<uint32_t>(kOut))
@@ -450,13 +533,20 @@ __device__ __forceinline__ void down_epilogue(const GemvArgs &a, const float *ti
         (wsum[4 * tid] + wsum[4 * tid + 1]) + (wsum[4 * tid + 2] + wsum[4 * tid + 3]);
 }
 
-// Consumer warp q (0..7) of the warps that computed half h of a tile.  Q8:
-// warp w covers block w % 8 of half w / 8; twin: warp w covers columns
-// 16 (w / 8) .. 16 (w / 8) + 15 of block w % 4 in half (w / 4) % 2.
-template <Fmt F>
-__device__ __forceinline__ int red_warp(int q, int h) {
-  if constexpr (F == Fmt::Q8) return 8 * h + q;
-  else return (q >> 2) * 8 + h * 4 + (q & 3);
+// Sum over the kRedWarps warps that computed element (s, row) of the parked
+// tile in slot sl (red[sl][warp][s][row % 64]), as a fixed tree.  Q8: warp
+// w computed block w % 8 for the rows of half w / 8.  Twin: warp w computed
+// columns 16 (w / 8) .. 16 (w / 8) + 15 of block w % 4 for the rows of half
+// (w / 4) % 2.
+template <Fmt F, int kOut>
+__device__ __forceinline__ float warp_total(const float *red, int sl, int s, int row) {
+  float v[kRedWarps];
+#pragma unroll
+  for (int q = 0; q < kRedWarps; ++q) {
+    const int w = F == Fmt::Q8 ? 8 * (row >> 6) + q : (q >> 2) * 8 + (row >> 6) * 4 + (q & 3);
+    v[q] = red[((sl * 16 + w) * kOut + s) * 64 + (row & 63)];
+  }
+  return tree_sum(v);
 }
 
 // Total of element (s, row) of shared tile rb: the partials of its CTAs
@@ -514,84 +604,40 @@ __device__ __forceinline__ void run_epilogue(const GemvArgs &a, float *epi, int3
   else if constexpr (E == Epi::Down) down_epilogue<kOut>(a, epi, scale, scale + 4, rb, tid, threads);
 }
 
-// Finishes one or two row tiles of the CTA: tile k (row tile rb[k], deferred
+// Finishes one or two row tiles of the CTA: tile k (row tile rb[k], parked
 // warp sums in red slot sl[k]).  Each element's total is the tree sum of the 8
 // warps that computed it.  A tile no other CTA shares is written out directly
 // (Plain) or through the fused epilogue.  A shared tile's totals go to this
-// CTA's partial slot in the workspace.  With a.combine_in_kernel == 0 that is
-// all: a separate kernel (combine_tiles_kernel) adds the partials of every
-// shared tile once the GEMV has completed, so a CTA leaves the SM right after
-// its last tile.  Otherwise (the persistent decode pass, which has no kernel
-// boundary to wait on) one fence and one ticket per tile follow, both tiles
-// in the same round, and the last CTA to arrive at a tile adds its partials.
-// Not inlined: it runs a few times per CTA, and one shared copy keeps the
-// consumer loops' instruction footprint small.
+// CTA's partial slot in the workspace, and a separate kernel
+// (combine_tiles_kernel) adds the partials of every shared tile once the GEMV
+// has completed, so a CTA leaves the SM right after its last tile.  Not
+// inlined: it runs a few times per CTA, and one shared copy keeps the consumer
+// loops' instruction footprint small.
 template <Fmt F, int N, Epi E>
 __device__ __noinline__ void finish_tiles(const GemvArgs &a, const float *red, int count, int32_t rb0, int sl0,
-                                          int32_t rb1, int sl1, uint32_t tid, volatile uint32_t *flag, float *epi) {
+                                          int32_t rb1, int sl1, uint32_t tid, float *epi) {
   using T = Traits<F, N>;
   constexpr int kOut = T::kOut;
   constexpr int kConsumerThreads = T::kWarps * 32;
   const int32_t rbs[2] = {rb0, rb1};
   const int sls[2] = {sl0, sl1};
-  int32_t clo[2] = {0, 0}, chi[2] = {0, 0};
-  bool any_shared = false;
+  bool epilogue_ran = false;
   for (int k = 0; k < count; ++k) {
-    clo[k] = cta_of_unit(static_cast<int64_t>(rbs[k]) * a.n_sb, a.units, a.grid);
-    chi[k] = cta_of_unit(static_cast<int64_t>(rbs[k] + 1) * a.n_sb - 1, a.units, a.grid);
-    any_shared = any_shared || chi[k] > clo[k];
-  }
-  auto warp_total = [&](int k, int s, int row) {
-    float v[T::kWarps / 2];
-#pragma unroll
-    for (int q = 0; q < T::kWarps / 2; ++q)
-      v[q] = red[((sls[k] * T::kWarps + red_warp<F>(q, row >> 6)) * kOut + s) * 64 + (row & 63)];
-    return tree_sum(v);
-  };
-  // ---- shared tiles: publish this CTA's partials
-  uint32_t last_bits = 0;
-  if (any_shared) {
-    for (int k = 0; k < count; ++k) {
-      if (chi[k] == clo[k]) continue;
+    const int32_t clo = cta_of_unit(static_cast<int64_t>(rbs[k]) * a.n_sb, a.units, a.grid);
+    const int32_t chi = cta_of_unit(static_cast<int64_t>(rbs[k] + 1) * a.n_sb - 1, a.units, a.grid);
+    if (chi > clo) {  // shared tile: publish this CTA's partials
       for (int t = tid; t < kOut * kRowsPerTile; t += kConsumerThreads) {
         const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
         a.part[((static_cast<int64_t>(blockIdx.x) * 2 + sls[k]) * kOut + s) * kRowsPerTile + row] =
-            warp_total(k, s, row);
+            warp_total<F, kOut>(red, sls[k], s, row);
       }
+      continue;
     }
-    if (a.combine_in_kernel) {
-      __threadfence();
-      named_barrier(kBarConsumers, kConsumerThreads);
-      if (tid == 0) {
-        uint32_t bits = 0;
-        for (int k = 0; k < count; ++k) {
-          if (chi[k] == clo[k]) continue;
-          const unsigned int prev = atomicAdd(&a.tickets[rbs[k]], 1u);
-          if (prev == static_cast<unsigned int>(chi[k] - clo[k])) {
-            a.tickets[rbs[k]] = 0u;  // ready for the next phase
-            bits |= 1u << k;
-          }
-        }
-        if (bits != 0u) __threadfence();
-        flag[1] = bits;
-      }
-      named_barrier(kBarConsumers, kConsumerThreads);
-      last_bits = flag[1];
-    }
-  }
-  // ---- write out the tiles this CTA completes
-  bool epilogue_ran = false;
-  for (int k = 0; k < count; ++k) {
-    const bool shared_tile = chi[k] > clo[k];
-    if (shared_tile && ((last_bits >> k) & 1u) == 0u) continue;
     if constexpr (E != Epi::Plain)
       if (epilogue_ran) named_barrier(kBarConsumers, kConsumerThreads);  // tile_out and wsum are reused
     for (int t = tid; t < kOut * kRowsPerTile; t += kConsumerThreads) {
       const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
-      const float total =
-          shared_tile ? sum_partials<kOut>(a, clo[k], chi[k], partial_slot_of_first(rbs[k], clo[k], a), s, row)
-                      : warp_total(k, s, row);
-      deliver<F, N, E>(a, epi, rbs[k], s, row, total);
+      deliver<F, N, E>(a, epi, rbs[k], s, row, warp_total<F, kOut>(red, sls[k], s, row));
     }
     if constexpr (E != Epi::Plain) {
       named_barrier(kBarConsumers, kConsumerThreads);
@@ -639,9 +685,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_tiles_kernel(const __
 // Shared-memory layout and identity of a consumer thread.
 struct ConsumerCtx {
   uint8_t *base_ptr;        // ring of stages
-  float *red;               // [2 slots][warps][kOut][64] deferred warp sums
+  float *red;               // [2 slots] parked warp sums (Stage::kRedBytes)
   float *epi;               // fused-epilogue scratch
-  volatile uint32_t *flag;  // [0] abort, [1] last-arriver flag
+  volatile uint32_t *flag;  // [0] abort
   uint32_t bars, flags;     // shared addresses of the barriers and flags
   uint32_t sq_bar;          // fused epilogues: completes when the input's per-tile sums are staged
   uint32_t sq_stage;        // shared address of the staged sums
@@ -650,18 +696,17 @@ struct ConsumerCtx {
   int64_t u0, u1;           // this CTA's unit range
 };
 
-// The consumer warps' walk over the CTA's units: wait for each stage, run
-// `body` on it (the warp's share of the unit), release the stage; at the end
-// of each row tile park the warp's sums, and finish the tiles.
-template <Fmt F, int N, Epi E, class Body, class Release>
-__device__ __forceinline__ void consumer_loop(const GemvArgs &a, const ConsumerCtx &c, Body &&body, Release &&release) {
+// The consumer warps' walk over the CTA's units: wait for each stage, run the
+// consumer `cons` on it (the warp's share of the unit), release the stage; at
+// the end of each row tile park the warp's sums, and finish the tiles.
+template <Fmt F, int N, Epi E, class Cons>
+__device__ __forceinline__ void consumer_loop(const GemvArgs &a, const ConsumerCtx &c, Cons &cons) {
   using T = Traits<F, N>;
   using S = Stage<F, N>;
   constexpr int kOut = T::kOut;
   constexpr int kConsumerThreads = T::kWarps * 32;
-  uint64_t acc[kTaskSlots][kOut];
-  uint32_t st = 0, ph = 0;  // ring slot and phase parity of unit i
-  int64_t i = 0;
+  const uint64_t limit = wait_limit(a);
+  uint32_t st = 0, ph = 0;  // ring slot and phase parity of the current unit
   // The fused epilogues need the input scales.  The producer stages the
   // input's per-tile sums in shared memory right after its wait on the
   // previous kernel; warp s < kOut derives scale s from them when the first
@@ -674,7 +719,7 @@ __device__ __forceinline__ void consumer_loop(const GemvArgs &a, const ConsumerC
     if (scales_ready) return;
     scales_ready = true;
     const bool staged = staged_sum_bytes<kOut>(a) != 0u;
-    if (staged && !mbar_try_wait(c.sq_bar, 0) && !mbar_wait_bounded(c.sq_bar, 0, c.flags)) {
+    if (staged && !mbar_try_wait(c.sq_bar, 0) && !mbar_wait_bounded(c.sq_bar, 0, c.flags, limit)) {
       if (c.flag[0] == 0) atomicOr(&g_device_error, PTI_DEVERR_FULL_TIMEOUT);
       c.flag[0] = 1;
       return;
@@ -689,16 +734,12 @@ __device__ __forceinline__ void consumer_loop(const GemvArgs &a, const ConsumerC
   for (int32_t rb = rb_first; rb <= rb_last; ++rb) {
     const int32_t sb_begin = (rb == rb_first) ? static_cast<int32_t>(c.u0 - static_cast<int64_t>(rb) * a.n_sb) : 0;
     const int32_t sb_end = (rb == rb_last) ? static_cast<int32_t>(c.u1 - static_cast<int64_t>(rb) * a.n_sb) : a.n_sb;
-#pragma unroll
-    for (int r = 0; r < kTaskSlots; ++r)
-#pragma unroll
-      for (int s = 0; s < kOut; ++s) acc[r][s] = 0ull;
-
-    for (int32_t sb = sb_begin; sb < sb_end; ++sb, ++i) {
+    cons.reset();
+    for (int32_t sb = sb_begin; sb < sb_end; ++sb) {
       const uint32_t full = c.bars + 8 * st;
       bool ok = mbar_try_wait(full, ph);
       if (!ok) {
-        ok = c.flag[0] == 0 && mbar_wait_bounded(full, ph, c.flags);
+        ok = c.flag[0] == 0 && mbar_wait_bounded(full, ph, c.flags, limit);
         if (!ok && c.flag[0] == 0) {
           atomicOr(&g_device_error, PTI_DEVERR_FULL_TIMEOUT);
           c.flag[0] = 1;
@@ -706,11 +747,10 @@ __device__ __forceinline__ void consumer_loop(const GemvArgs &a, const ConsumerC
       }
       if (ok) {
         const uint8_t *tile = c.base_ptr + st * S::kBytes;
-        body(tile, tile + kStageBytes, i, acc);
+        cons.template unit<S::kXStreamBytes>(tile, tile + kStageBytes);
       }
       __syncwarp();
       if (c.lane == 0) mbar_arrive(c.bars + 8 * (c.stages + st));
-      release(i, st, ph);
       if (++st == static_cast<uint32_t>(c.stages)) {
         st = 0;
         ph ^= 1u;
@@ -720,27 +760,20 @@ __device__ __forceinline__ void consumer_loop(const GemvArgs &a, const ConsumerC
     // ---- park this warp's sums for the tile: slot 0 = first tile of the CTA,
     //      slot 1 = any later one (only the last can be shared with another CTA)
     const int sl = (rb == rb_first) ? 0 : 1;
-    const bool middle = rb != rb_first && rb != rb_last;
-#pragma unroll
-    for (int r = 0; r < kTaskSlots; ++r)
-#pragma unroll
-      for (int s = 0; s < kOut; ++s) {
-        const float2 v = unpack2(acc[r][s]);
-        c.red[((sl * T::kWarps + c.warp) * kOut + s) * 64 + r * 32 + c.lane] = v.x + v.y;
-      }
-    if (middle) {
+    cons.template park<kOut>(c.red, sl, c.warp);
+    if (rb != rb_first && rb != rb_last) {
       // a tile wholly inside this CTA's range: finish it now (when a CTA
       // spans more than two row tiles, as most gate/up CTAs of the decode
       // pass do: 20 units per tile, about 36 per CTA)
       wait_scales();
       named_barrier(kBarConsumers, kConsumerThreads);
-      finish_tiles<F, N, E>(a, c.red, 1, rb, 1, 0, 0, c.tid, c.flag, c.epi);
+      finish_tiles<F, N, E>(a, c.red, 1, rb, 1, 0, 0, c.tid, c.epi);
       named_barrier(kBarConsumers, kConsumerThreads);
     }
   }
   wait_scales();
   named_barrier(kBarConsumers, kConsumerThreads);
-  finish_tiles<F, N, E>(a, c.red, rb_last != rb_first ? 2 : 1, rb_first, 0, rb_last, 1, c.tid, c.flag, c.epi);
+  finish_tiles<F, N, E>(a, c.red, rb_last != rb_first ? 2 : 1, rb_first, 0, rb_last, 1, c.tid, c.epi);
 }
 
 // The copy side of the ring, run by lane 0 of the producer warp: it fills the
@@ -834,7 +867,7 @@ struct Producer {
     issued = first;
     for (int64_t i = first; i < pre; ++i) {
       const uint32_t landed = bars + 8 * static_cast<uint32_t>(i - ramp);
-      if (!mbar_try_wait(landed, 0) && !mbar_wait_bounded(landed, 0, flags)) {
+      if (!mbar_try_wait(landed, 0) && !mbar_wait_bounded(landed, 0, flags, wait_limit(*a))) {
         if (flag[0] == 0) atomicOr(&g_device_error, PTI_DEVERR_FULL_TIMEOUT);
         flag[0] = 1;
         return;
@@ -846,12 +879,14 @@ struct Producer {
     }
   }
   // Once every consumer warp has released unit i (ring slot st, phase parity
-  // ph), fetch unit i + stages into the slot.
+  // ph), fetch unit i + stages into the slot.  (Testing: CTA 0 issues nothing
+  // from unit a->stall_unit on.)
   __device__ __forceinline__ void refill(int64_t i, uint32_t st, uint32_t ph) {
     const int64_t j = i + stages;
     if (j >= nu || flag[0] != 0) return;
+    if (a->stall_unit >= 0 && j >= a->stall_unit && blockIdx.x == 0) return;
     const uint32_t empty = bars + 8 * (stages + st);
-    if (!mbar_try_wait(empty, ph) && !mbar_wait_bounded(empty, ph, flags)) {
+    if (!mbar_try_wait(empty, ph) && !mbar_wait_bounded(empty, ph, flags, wait_limit(*a))) {
       if (flag[0] == 0) atomicOr(&g_device_error, PTI_DEVERR_EMPTY_TIMEOUT);
       flag[0] = 1;
       return;
@@ -878,16 +913,15 @@ __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
                     const __grid_constant__ GemvArgs a) {
   using T = Traits<F, N>;
   using S = Stage<F, N>;
-  constexpr int kOut = T::kOut;
   constexpr int kConsumerWarps = T::kWarps;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *const base_ptr = smem_raw + (base - raw);
   const int stages = a.stages;
-  float *const red = reinterpret_cast<float *>(base_ptr + stages * S::kBytes);  // [2][warps][kOut][64]
+  float *const red = reinterpret_cast<float *>(base_ptr + stages * S::kBytes);  // parked warp sums
   const uint32_t bars = base + stages * S::kBytes + S::kRedBytes;             // full[stages], empty[stages]
-  const uint32_t flags = bars + 2 * stages * 8;  // flag words [0], [1]; then the barrier of the staged sums
+  const uint32_t flags = bars + 2 * stages * 8;  // abort flag, a spare word; then the barrier of the staged sums
   const uint32_t sq_bar = flags + 8;
   volatile uint32_t *const flag = reinterpret_cast<volatile uint32_t *>(base_ptr + (flags - base));
   float *const epi = reinterpret_cast<float *>(base_ptr + (flags - base) + 16);  // kEpiBytes (fused epilogues)
@@ -931,45 +965,27 @@ __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
 
   // ---------------- consumers ----------------------------------------------
   const ConsumerCtx cx{base_ptr, red, epi, flag, bars, flags, sq_bar, sq_stage, stages, tid, warp, lane, u0, u1};
-  auto release = [](int64_t, uint32_t, uint32_t) {};
+  auto run = [&](auto cons) {
+    cons.init(warp, lane);
+    consumer_loop<F, N, E>(a, cx, cons);
+  };
   if constexpr (F == Fmt::Q8) {
-    // Warp w always computes block b = w % 8 of every unit for the rows of half
-    // w / 8; the warps of a scheduler (w % 4) share the parity of b and so
-    // run one code body.
-    const uint32_t half = warp >> 3, blk = warp & 7u;
-    const uint32_t win_off = 32u * blk;
-    const bool c_hi = (blk & 4u) != 0u;
-    auto run = [&](auto ec, auto cc) {
-      constexpr int E_ = decltype(ec)::value;
-      constexpr int C_ = decltype(cc)::value;
-      consumer_loop<F, N, E>(a, cx, [&](const uint8_t *tile, const uint8_t *xsb, int64_t,
-                                        uint64_t (&acc)[kTaskSlots][kOut]) {
-        q8_block_body<N, E_, C_>(tile, xsb + 128u * blk, lane, half, win_off, c_hi, acc);
-      }, release);
-    };
-    switch (blk & 3u) {  // = warp % 4: one code body per scheduler
-      case 0: run(std::integral_constant<int, 0>{}, std::integral_constant<int, 0>{}); break;
-      case 1: run(std::integral_constant<int, 1>{}, std::integral_constant<int, 0>{}); break;
-      case 2: run(std::integral_constant<int, 0>{}, std::integral_constant<int, 1>{}); break;
-      default: run(std::integral_constant<int, 1>{}, std::integral_constant<int, 1>{}); break;
+    // Warp w computes block w % 8; the warps of a scheduler (w % 4) share the
+    // parity of the block and so run one code body.
+    switch (warp & 3u) {  // block b = 2c + e: (e, c % 2)
+      case 0: run(Q8Pair<N, 0, 0>{}); break;
+      case 1: run(Q8Pair<N, 1, 0>{}); break;
+      case 2: run(Q8Pair<N, 0, 1>{}); break;
+      default: run(Q8Pair<N, 1, 1>{}); break;
     }
   } else {
-    // Twin: warp w computes block b = w % 4 (its scheduler, so one code body
-    // per scheduler) of every unit, columns 16 ch .. 16 ch + 15 of the block
-    // (ch = w / 8), for the rows of half (w / 4) % 2.
-    const uint32_t half = (warp >> 2) & 1u, ch = warp >> 3;
-    auto run = [&](auto bc) {
-      constexpr int B_ = decltype(bc)::value;
-      consumer_loop<F, N, E>(a, cx, [&](const uint8_t *tile, const uint8_t *xsb, int64_t,
-                                        uint64_t (&acc)[kTaskSlots][kOut]) {
-        twin_block_body<N, B_>(tile, xsb, lane, half, ch, acc);
-      }, release);
-    };
+    // Twin: warp w computes block w % 4 (its scheduler, so one code body per
+    // scheduler).
     switch (warp & 3u) {
-      case 0: run(std::integral_constant<int, 0>{}); break;
-      case 1: run(std::integral_constant<int, 1>{}); break;
-      case 2: run(std::integral_constant<int, 2>{}); break;
-      default: run(std::integral_constant<int, 3>{}); break;
+      case 0: run(TwinSlab<N, 0>{}); break;
+      case 1: run(TwinSlab<N, 1>{}); break;
+      case 2: run(TwinSlab<N, 2>{}); break;
+      default: run(TwinSlab<N, 3>{}); break;
     }
   }
 }
@@ -1050,7 +1066,7 @@ bool encode_weight_map(CUtensorMap *tmap, const void *w, int64_t rows, int64_t c
 }
 
 // Launches the persistent kernel.  `a` carries the operands (x0, x1, y0, y1,
-// part, tickets, rows, cols and the epilogue fields); the tiling fields are
+// part, rows, cols and the epilogue fields); the tiling fields are
 // filled in here.  w2 is the up matrix of a GateUp launch.  With `pdl` the
 // launch may start while the previous kernel in the stream is still running
 // (programmatic dependent launch); the kernel reads only weights before it
@@ -1090,7 +1106,6 @@ pti_status launch_gemv(const void *w, const void *w2, GemvArgs a, cudaStream_t s
   a.n_rb = static_cast<int32_t>(p.n_rb);
   a.grid = p.grid;
   a.stages = p.stages;
-  a.combine_in_kernel = 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
   cfg.blockDim = dim3(T::kWarps * 32 + 32);
@@ -1116,11 +1131,14 @@ pti_status launch_gemv(const void *w, const void *w2, GemvArgs a, cudaStream_t s
   return launch_status();
 }
 
-// The plain GEMV: partials at the start of the workspace, tickets after them.
+// The plain GEMV: the workspace holds the shared tiles' partials.
 template <Fmt F, int N>
 pti_status launch_fast(const void *w, int64_t rows, int64_t cols, const float *x0, const float *x1,
-                       float *y0, float *y1, void *workspace, cudaStream_t stream, bool pdl = false) {
+                       float *y0, float *y1, void *workspace, cudaStream_t stream, bool pdl = false,
+                       uint64_t wait_ns = 0, int64_t stall_unit = -1) {
   GemvArgs a = {};
+  a.wait_ns = wait_ns;
+  a.stall_unit = stall_unit;
   a.x0 = x0;
   a.x1 = x1;
   a.y0 = y0;

@@ -187,14 +187,27 @@ def test_ex_entry_points_reject_unknown_flags(L):
     assert L.pti_ssq_twin_gemv_ex(None, *targs[1:], 1) == 1
 
 
-def test_decode_pass_ex_rejects_unknown_flags(L):
+def test_decode_pass_layer_count(L):
     ok_bytes = L.pti_mlp_decode_pass_workspace_bytes(512, 1024, 4)
     gate, up, down = _ptrs(GATE), _ptrs(UP), _ptrs(DOWN)
-    args = (gate, up, down, 1, 512, 1024, 4, 1e-6, FAKE + (8 << 34), FAKE + (9 << 34), FAKE + (10 << 34),
-            ok_bytes, None)
-    assert L.pti_mlp_decode_pass_ex(*args, 1) == 8 and L.pti_mlp_decode_pass_ex(*args, 4) == 8
-    assert L.pti_mlp_decode_pass_ex(gate, up, down, 0, *args[4:], 2) == 2
-    assert L.pti_mlp_decode_pass_ex(gate, up, down, 4097, *args[4:], 0) == 2
+    args = (512, 1024, 4, 1e-6, FAKE + (8 << 34), FAKE + (9 << 34), FAKE + (10 << 34), ok_bytes, None)
+    assert L.pti_mlp_decode_pass(gate, up, down, 0, *args) == 2
+    assert L.pti_mlp_decode_pass(gate, up, down, 4097, *args) == 2
+
+
+def test_stall_hook_validation(L):
+    """The testing hook checks its arguments like the GEMV (nothing launched)."""
+    x, y, ws = FAKE + (1 << 30), FAKE + (2 << 30), FAKE + (3 << 30)
+
+    def call(w=FAKE, rows=1024, cols=512, n=2, x=x, y=y, ws=ws, ws_bytes=1 << 24, stall=8, wait=10 ** 6):
+        return L.pti_test_q8_gemv_stall(w, rows, cols, n, x, y, ws, ws_bytes, None, stall, wait)
+
+    assert call(w=None) == 1 and call(ws=None) == 1
+    assert call(cols=96) == 2 and call(cols=128) == 2           # the hook needs the fast path
+    assert call(n=5) == 3
+    assert call(x=x + 4) == 4 and call(ws=ws + 16) == 4
+    assert call(ws_bytes=256) == 7
+    assert call(wait=999) == 8 and call(wait=3 * 10 ** 9) == 8
 
 
 def test_twin_nstream_validation(L):

@@ -92,22 +92,22 @@ def check_layer(got, xo, tol, what):
         raise AssertionError(f"{what}: {(err > tol).sum()} outputs off; worst {i}: err {err[i]:.3g}, bar {tol[i]:.3g}")
 
 
-def run_pass(weights, n_layers, hidden, ffn, x, eps=EPS, persistent=False):
+def run_pass(weights, n_layers, hidden, ffn, x, eps=EPS):
     w = pti.DecodeWeights(weights.tensors[0][:n_layers], weights.tensors[1][:n_layers],
                           weights.tensors[2][:n_layers])
-    y = pti.mlp_decode_pass(w, hidden, ffn, x, eps=eps, persistent=persistent)
+    y = pti.mlp_decode_pass(w, hidden, ffn, x, eps=eps)
     torch.cuda.synchronize()
     return y.cpu().numpy()
 
 
-def check_chain(layers, hidden, ffn, n, seed, eps=EPS, x=None, persistent=False):
+def check_chain(layers, hidden, ffn, n, seed, eps=EPS, x=None):
     w = device_weights(layers)
     if x is None:
         x = pti_synth.activations(n, hidden, seed, 1000)
     xd = dev(x)
     prev = x.astype(np.float64)
     for k in range(1, len(layers) + 1):
-        got = run_pass(w, k, hidden, ffn, xd, eps, persistent)
+        got = run_pass(w, k, hidden, ffn, xd, eps)
         xo, tol = layer_tolerance(*layers[k - 1], hidden, ffn, prev.astype(np.float32), eps)
         check_layer(got, xo, tol, f"hidden {hidden} ffn {ffn} n {n} layer {k}")
         prev = got.astype(np.float64)
@@ -117,35 +117,33 @@ def check_chain(layers, hidden, ffn, n, seed, eps=EPS, x=None, persistent=False)
 # shapes: stream-K tiles shared by several CTAs (256x512, 768x1280), whole
 # tiles per CTA in the down kernel (4096x256), CTAs spanning more than two
 # gate/up tiles (256x40960)
-@pytest.mark.parametrize("persistent", [False, True])
 @pytest.mark.parametrize("hidden,ffn", [(256, 512), (768, 1280), (4096, 256), (256, 40960)])
 @pytest.mark.parametrize("n", [1, 2, 3, 4])
-def test_decode_pass_one_layer(hidden, ffn, n, persistent):
+def test_decode_pass_one_layer(hidden, ffn, n):
     layers = host_layers(1, hidden, ffn, seed=hidden + ffn)
-    check_chain(layers, hidden, ffn, n, seed=n, persistent=persistent)
+    check_chain(layers, hidden, ffn, n, seed=n)
 
 
-@pytest.mark.parametrize("persistent", [False, True])
 @pytest.mark.parametrize("n", [1, 4])
-def test_decode_pass_three_layers(n, persistent):
+def test_decode_pass_three_layers(n):
     hidden, ffn = 512, 1536
     layers = host_layers(3, hidden, ffn, seed=5)
-    check_chain(layers, hidden, ffn, n, seed=7, persistent=persistent)
+    check_chain(layers, hidden, ffn, n, seed=7)
 
 
-def test_decode_pass_more_layers_than_one_launch_holds():
-    """70 layers: the persistent form splits them over two launches (64 + 6);
-    the layers on both sides of the launch boundary and the last one stay
-    within their bars."""
+def test_decode_pass_seventy_layers():
+    """70 chained layers: layers 64, 65 and 70 each stay within their bars
+    (the pass over k layers against the oracle's layer k applied to the pass's
+    own output after k - 1)."""
     hidden, ffn, n = 256, 512, 2
     layers = host_layers(70, hidden, ffn, seed=31)
     x = pti_synth.activations(n, hidden, 31, 1000)
     w = device_weights(layers)
     for k in (64, 65, 70):
-        g_k = run_pass(w, k, hidden, ffn, dev(x), persistent=True)
-        g_prev = run_pass(w, k - 1, hidden, ffn, dev(x), persistent=True)
+        g_k = run_pass(w, k, hidden, ffn, dev(x))
+        g_prev = run_pass(w, k - 1, hidden, ffn, dev(x))
         xo, tol = layer_tolerance(*layers[k - 1], hidden, ffn, g_prev.astype(np.float32))
-        check_layer(g_k, xo, tol, f"persistent layer {k}")
+        check_layer(g_k, xo, tol, f"layer {k}")
 
 
 def test_decode_pass_eps_matters():
@@ -177,24 +175,23 @@ def test_decode_pass_64_layers(capsys):
               f"rms of the output {np.sqrt(np.mean(ref * ref)):.3g}")
 
 
-@pytest.mark.parametrize("persistent", [False, True])
-def test_decode_pass_is_deterministic_in_place_and_needs_no_workspace_init(persistent):
+def test_decode_pass_is_deterministic_in_place_and_needs_no_workspace_init():
     hidden, ffn, n = 768, 1280, 4
     layers = host_layers(2, hidden, ffn, seed=4)
     w = device_weights(layers)
     x = dev(pti_synth.activations(n, hidden, 4, 1000))
     need = pti.mlp_decode_pass_workspace_bytes(hidden, ffn, n)
     ws = torch.full((need + 4096,), 255, dtype=torch.uint8, device="cuda")  # NaN patterns everywhere
-    a = pti.mlp_decode_pass(w, hidden, ffn, x, ws=ws, persistent=persistent)
-    b = pti.mlp_decode_pass(w, hidden, ffn, x, ws=ws, persistent=persistent)
+    a = pti.mlp_decode_pass(w, hidden, ffn, x, ws=ws)
+    b = pti.mlp_decode_pass(w, hidden, ffn, x, ws=ws)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
     xi = x.clone()
-    pti.mlp_decode_pass(w, hidden, ffn, xi, x_out=xi, ws=ws, persistent=persistent)
+    pti.mlp_decode_pass(w, hidden, ffn, xi, x_out=xi, ws=ws)
     torch.cuda.synchronize()
     assert torch.equal(xi, a)
     xo, tol = layer_tolerance(*layers[1], hidden, ffn,
-                              run_pass(w, 1, hidden, ffn, x, persistent=persistent).astype(np.float32))
+                              run_pass(w, 1, hidden, ffn, x).astype(np.float32))
     check_layer(a.cpu().numpy(), xo, tol, "layer 2 on a garbage-filled workspace")
     # the same workspace then serves a plain GEMV of another shape
     wq = dev(pti_synth.q8_matrix(1000, 2048, 4, 77))
@@ -235,8 +232,7 @@ def test_decode_pass_full_size_two_layers():
     check_layer(got1, xo, tol, "full size layer 1")
     g, u, d = (t.cpu().numpy() for t in layers_dev[1])
     xo, tol = layer_tolerance(g, u, d, hidden, ffn, got1.astype(np.float32))
-    for persistent in (False, True):
-        got2 = run_pass(w, 2, hidden, ffn, xd, persistent=persistent)
-        check_layer(got2, xo, tol, f"full size layer 2 persistent={persistent}")
+    got2 = run_pass(w, 2, hidden, ffn, xd)
+    check_layer(got2, xo, tol, "full size layer 2")
     del layers_dev, w
     torch.cuda.empty_cache()
