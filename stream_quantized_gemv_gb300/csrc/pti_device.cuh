@@ -13,6 +13,8 @@ namespace pti {
 // A pipeline wait that has not completed after this long can only be a
 // hardware fault; the kernel then records an error and winds down.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+// Pause between the polls of the copy producer's bounded waits.
+constexpr uint32_t kProducerBackoffNs = 200u;
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
@@ -61,16 +63,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity (never suspends).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false if it
 // has not completed within `timeout_ns` (or 2^30 polls), or, when
 // `abort_flag` is a shared-memory address other than 0, as soon as the 32-bit
 // word there becomes non-zero (another warp of the CTA recorded an error).
+// `backoff_ns` > 0 pauses between polls, so that a warp that waits long (the
+// copy producer waiting for the consumers to free a slot) takes no issue
+// slots from the warps it shares a scheduler with.
 static __device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t abort_flag,
-                                                      uint64_t timeout_ns = kWaitTimeoutNs) {
+                                                      uint64_t timeout_ns = kWaitTimeoutNs, uint32_t backoff_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1; i < (1u << 30); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (backoff_ns != 0) __nanosleep(backoff_ns);
     if ((i & 63u) == 0) {
       if (globaltimer_ns() - t0 > timeout_ns) return false;
       if (abort_flag != 0) {

@@ -737,7 +737,7 @@ __device__ __forceinline__ void consumer_loop(const GemvArgs &a, const ConsumerC
     cons.reset();
     for (int32_t sb = sb_begin; sb < sb_end; ++sb) {
       const uint32_t full = c.bars + 8 * st;
-      bool ok = mbar_try_wait(full, ph);
+      bool ok = mbar_test_wait(full, ph);
       if (!ok) {
         ok = c.flag[0] == 0 && mbar_wait_bounded(full, ph, c.flags, limit);
         if (!ok && c.flag[0] == 0) {
@@ -793,44 +793,49 @@ struct Producer {
   int64_t u0, nu, issued;
   uint64_t pol;
   uint32_t sq_bar, sq_stage;  // fused epilogues: barrier and buffer of the staged input sums
+  // Row tile and super-block of the next unit whose weights (w) and
+  // activations (x) are to be fetched.  Copies are issued in unit order, so
+  // both cursors only step forward (no division per unit: the producer warp
+  // shares a scheduler with four consumer warps and every instruction it
+  // issues is taken from them).
+  int32_t w_rb, w_sb, x_sb;
 
-  __device__ __forceinline__ void coords(int64_t i, int32_t &rb, int32_t &sb) const {
-    const int64_t u = u0 + i;
-    rb = static_cast<int32_t>(u / a->n_sb);
-    sb = static_cast<int32_t>(u - static_cast<int64_t>(rb) * a->n_sb);
+  __device__ __forceinline__ void init_cursors() {
+    w_rb = static_cast<int32_t>(u0 / a->n_sb);
+    w_sb = static_cast<int32_t>(u0 - static_cast<int64_t>(w_rb) * a->n_sb);
+    x_sb = w_sb;
   }
-  __device__ __forceinline__ void load_w(int64_t i, uint32_t slot) const {
-    int32_t rb, sb;
-    coords(i, rb, sb);
+  __device__ __forceinline__ void load_w(uint32_t slot) {
     const uint32_t dst = base + slot * S::kBytes, bar = bars + 8 * slot;
     if constexpr (E == Epi::GateUp) {
-      tma_load_2d(dst, tmap, 34 * sb, rb * 64, bar, pol);
-      tma_load_2d(dst + 64 * kSBBytes, tmap2, 34 * sb, rb * 64, bar, pol);
+      tma_load_2d(dst, tmap, 34 * w_sb, w_rb * 64, bar, pol);
+      tma_load_2d(dst + 64 * kSBBytes, tmap2, 34 * w_sb, w_rb * 64, bar, pol);
     } else {
-      tma_load_2d(dst, tmap, 34 * sb, rb * kRowsPerTile, bar, pol);
+      tma_load_2d(dst, tmap, 34 * w_sb, w_rb * kRowsPerTile, bar, pol);
+    }
+    if (++w_sb == a->n_sb) {
+      w_sb = 0;
+      ++w_rb;
     }
   }
-  __device__ __forceinline__ void load_x(int64_t i, uint32_t slot) const {
-    int32_t rb, sb;
-    coords(i, rb, sb);
+  __device__ __forceinline__ void load_x(uint32_t slot) {
     const uint32_t xdst = base + slot * S::kBytes + kStageBytes, bar = bars + 8 * slot;
+    const int64_t col = static_cast<int64_t>(x_sb) * T::kColsPerSB;
     if constexpr (F == Fmt::Q8) {
 #pragma unroll
       for (int st = 0; st < N; ++st)
-        bulk_load(xdst + st * S::kXStreamBytes,
-                  a->x0 + static_cast<int64_t>(st) * a->cols + static_cast<int64_t>(sb) * T::kColsPerSB,
-                  S::kXStreamBytes, bar);
+        bulk_load(xdst + st * S::kXStreamBytes, a->x0 + static_cast<int64_t>(st) * a->cols + col, S::kXStreamBytes,
+                  bar);
     } else {
 #pragma unroll
       for (int st = 0; st < N; ++st) {
-        bulk_load(xdst + st * S::kXStreamBytes,
-                  a->x0 + static_cast<int64_t>(st) * a->cols + static_cast<int64_t>(sb) * T::kColsPerSB,
-                  S::kXStreamBytes, bar);
-        bulk_load(xdst + (N + st) * S::kXStreamBytes,
-                  a->x1 + static_cast<int64_t>(st) * a->cols + static_cast<int64_t>(sb) * T::kColsPerSB,
+        bulk_load(xdst + st * S::kXStreamBytes, a->x0 + static_cast<int64_t>(st) * a->cols + col, S::kXStreamBytes,
+                  bar);
+        bulk_load(xdst + (N + st) * S::kXStreamBytes, a->x1 + static_cast<int64_t>(st) * a->cols + col,
                   S::kXStreamBytes, bar);
       }
     }
+    if (++x_sb == a->n_sb) x_sb = 0;
   }
   // Weights do not depend on the previous kernel in the stream: fetch the
   // first tiles before waiting for it, then their activations.  When the
@@ -844,12 +849,13 @@ struct Producer {
   __device__ __forceinline__ void start() {
     prefetch_tmap(tmap);
     if constexpr (E == Epi::GateUp) prefetch_tmap(tmap2);
+    init_cursors();
     const int64_t ramp = (F == Fmt::Q8 && N >= 2 && !a->prefetch_all) ? 2 : kMaxStages;
     const int64_t pre = nu < stages ? nu : stages;
     const int64_t first = pre < ramp ? pre : ramp;
     for (int64_t i = 0; i < first; ++i) {
       mbar_expect_tx(bars + 8 * i, kStageBytes);
-      load_w(i, static_cast<uint32_t>(i));
+      load_w(static_cast<uint32_t>(i));
     }
     pdl_wait_primary();
     if constexpr (E != Epi::Plain) {
@@ -862,7 +868,7 @@ struct Producer {
     }
     for (int64_t i = 0; i < first; ++i) {
       mbar_arrive_expect_tx(bars + 8 * i, S::kXBytes);
-      load_x(i, static_cast<uint32_t>(i));
+      load_x(static_cast<uint32_t>(i));
     }
     issued = first;
     for (int64_t i = first; i < pre; ++i) {
@@ -873,8 +879,8 @@ struct Producer {
         return;
       }
       mbar_arrive_expect_tx(bars + 8 * i, kStageBytes + S::kXBytes);
-      load_w(i, static_cast<uint32_t>(i));
-      load_x(i, static_cast<uint32_t>(i));
+      load_w(static_cast<uint32_t>(i));
+      load_x(static_cast<uint32_t>(i));
       issued = i + 1;
     }
   }
@@ -886,14 +892,14 @@ struct Producer {
     if (j >= nu || flag[0] != 0) return;
     if (a->stall_unit >= 0 && j >= a->stall_unit && blockIdx.x == 0) return;
     const uint32_t empty = bars + 8 * (stages + st);
-    if (!mbar_try_wait(empty, ph) && !mbar_wait_bounded(empty, ph, flags, wait_limit(*a))) {
+    if (!mbar_try_wait(empty, ph) && !mbar_wait_bounded(empty, ph, flags, wait_limit(*a), kProducerBackoffNs)) {
       if (flag[0] == 0) atomicOr(&g_device_error, PTI_DEVERR_EMPTY_TIMEOUT);
       flag[0] = 1;
       return;
     }
     mbar_arrive_expect_tx(bars + 8 * st, kStageBytes + S::kXBytes);
-    load_w(j, st);
-    load_x(j, st);
+    load_w(st);
+    load_x(st);
     issued = j + 1;
   }
   // Stay until every copy issued into this CTA's shared memory has landed
@@ -948,7 +954,7 @@ __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
     // ---------------- producer: one lane issues every copy --------------------
     if (lane == 0) {
       Producer<F, N, E> prod{&tmap, &tmap2, &a, base, bars, flags, flag, stages, u0, u1 - u0, 0,
-                             l2_policy_evict_first(), sq_bar, sq_stage};
+                             l2_policy_evict_first(), sq_bar, sq_stage, 0, 0, 0};
       prod.start();
       uint32_t st = 0, ph = 0;
       for (int64_t i = 0; i + stages < prod.nu && flag[0] == 0; ++i) {
