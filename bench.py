@@ -175,14 +175,15 @@ class Q8Pass:
     """N-stream Q8 GEMV over L distinct rows x cols matrices (one step = one pass)."""
     sources = GEMV_SOURCES
 
-    def __init__(self, rows=17408, cols=5120, n=4, layers=16, seed=0):
+    def __init__(self, rows=17408, cols=5120, n=4, layers=16, seed=0, w=None):
         import torch
         import pti_synth
         import stream_quantized_gemv_gb300 as pti
         self.pti, self.torch = pti, torch
         self.rows, self.cols, self.n, self.layers = rows, cols, n, layers
         self.name = f"q8_gemv_n{n}_{rows}x{cols}_x{layers}"
-        self.w = [pti_synth.q8_matrix_device(rows, cols, seed, 1000 + i) for i in range(layers)]
+        self.w = w if w is not None else [pti_synth.q8_matrix_device(rows, cols, seed, 1000 + i)
+                                          for i in range(layers)]
         self.x = pti_synth.activations_device(n, cols, seed, 1)
         self.y = torch.empty((n, rows), dtype=torch.float32, device="cuda")
         need = pti.q8_gemv_workspace_bytes(rows, cols, n)
@@ -632,17 +633,70 @@ def time_e2e(wl, steps, warmup):
     return ms, sum(h.numel() * h.element_size() for h, _ in ins), hy.numel() * hy.element_size()
 
 
-def time_cpu(wl, budget_s=12.0):
+def host_cores() -> int:
+    """Host cores online (sysconf), the thread count of the all-core oracle."""
+    try:
+        return int(os.sysconf("SC_NPROCESSORS_ONLN"))
+    except (ValueError, OSError, AttributeError):
+        return os.cpu_count() or 1
+
+
+def time_cpu(wl, budget_s=8.0):
+    """The oracle on a bounded sample of the workload: single-threaded, and with
+    its row loops split over all host cores (OpenMP build of the same source).
+    Returns (all-core GB/s, cores, single-core GB/s, sample description,
+    seconds per sample on all cores)."""
+    import oracle
     run, sample_bytes, what = wl.cpu_sample()
-    t0 = time.perf_counter()
-    run()
-    one = time.perf_counter() - t0
-    reps = max(1, min(100000, int(budget_s / max(one, 1e-6))))
-    t0 = time.perf_counter()
-    for _ in range(reps):
+
+    def rate():
+        t0 = time.perf_counter()
         run()
-    dt = (time.perf_counter() - t0) / reps
-    return sample_bytes / dt / 1e9, what, dt
+        one = time.perf_counter() - t0
+        reps = max(1, min(100000, int(budget_s / max(one, 1e-6))))
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            run()
+        return (time.perf_counter() - t0) / reps
+
+    oracle.use_all_cores(False)
+    dt1 = rate()
+    cores = 1
+    dtn = dt1
+    if oracle.has_all_cores():
+        oracle.use_all_cores(True)
+        try:
+            dtn = rate()
+            cores = host_cores()
+        finally:
+            oracle.use_all_cores(False)
+    return sample_bytes / dtn / 1e9, cores, sample_bytes / dt1 / 1e9, what, dtn
+
+
+def q8_target(a, world, local, peak, peak_kind):
+    """The 4-stream Q8 GEMV on 17408 x 5120 against the 1-stream one, in the
+    same harness (16 distinct matrices per step, launches after the first
+    chained by programmatic dependent launch, CUDA-graph replay): time per
+    GEMV, effective GB/s, fractions of the measured and the nominal HBM rate,
+    and the step-time ratio N=4 / N=1."""
+    import torch
+    out = {"shape": "17408x5120", "matrices_per_step": 16, "steps": a.steps}
+    shared = None
+    for n in (1, 4):
+        wl = Q8Pass(17408, 5120, n, 16, w=shared)
+        shared = wl.w
+        ms, clocks = time_gpu(wl, a.steps, a.warmup, world, local)
+        us = ms * 1e3 / wl.layers
+        gbs = wl.launch_bytes / (us * 1e-6) / 1e9
+        out[f"n{n}"] = {"us_per_gemv": round(us, 3), "gbs": round(gbs, 1),
+                        "of_measured": round(gbs / peak, 4), "of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+                        "stream_tokens_per_s": round(n / (us * 1e-6), 1), "clocks": clocks}
+        del wl
+    out["ratio_n4_over_n1"] = round(out["n4"]["us_per_gemv"] / out["n1"]["us_per_gemv"], 4)
+    out["peak_kind"] = peak_kind
+    del shared
+    torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -661,6 +715,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--vsteps", type=int, default=4096, help="steps of the verify batches")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-q8-target", action="store_true",
+                    help="decode line: skip the 17408x5120 Q8 GEMV timing at N = 1 and N = 4")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
 
@@ -675,6 +731,10 @@ def main():
         for name in names:
             wl = _cpu_only_workload(name, a)
             run, sample_bytes, what = wl.cpu_sample()
+            cores = 1
+            if oracle.has_all_cores():
+                oracle.use_all_cores(True)
+                cores = host_cores()
             for _ in range(a.warmup):
                 run()
             t0 = time.perf_counter()
@@ -687,7 +747,7 @@ def main():
                     "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                     "dtype": "f64", "data": "synthetic", "impl": "reference",
                     "config": wl.config(),
-                    "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                    "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                      "sample": what},
                     "e2e": {"value": round(v, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
                             "d2h_bytes_per_step": 0}}
@@ -739,12 +799,16 @@ def main():
                                     "frac": round(fma_rate / fma_peak, 4),
                                     "peak_derivation": f"128 FP32 lanes x {sms} SMs x {mhz:.0f} MHz",
                                     "ops": "per weight: N product FMAs + 1 dequantising FMA"}
+        if name == "decode" and not a.no_q8_target:
+            line["q8_target"] = q8_target(a, world, local, peak, peak_kind)
         if rank == 0 and world == 1 and not a.no_cpu_baseline:
             import oracle
             oracle.build()
-            v, what, dt = time_cpu(wl)
-            line["cpu_baseline"] = {"value": round(v, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                    "sample": what, "seconds_per_sample": round(dt, 4)}
+            v, cores, v1, what, dt = time_cpu(wl)
+            line["cpu_baseline"] = {"value": round(v, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                    "sample": what, "seconds_per_sample": round(dt, 4),
+                                    "single_core_value": round(v1, 6),
+                                    "threads": "row loops split over all host cores (OpenMP build of the oracle)"}
         if rank == 0:
             print(json.dumps(line), flush=True)
         del wl

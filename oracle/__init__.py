@@ -32,23 +32,57 @@ TWIN_BLOCK_BYTES = 68
 BLOCK_COLS = 32
 
 
-def _stale() -> bool:
-    if not os.path.exists(_LIB_PATH):
+_OMP_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle_omp.so")
+
+
+def _stale_lib(path: str) -> bool:
+    if not os.path.exists(path):
         return True
-    built = os.path.getmtime(_LIB_PATH)
+    built = os.path.getmtime(path)
     return any(os.path.getmtime(p) > built for p in _SOURCES + _HEADERS)
 
 
+def _compile(path: str, extra: list[str]) -> None:
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    tmp = path + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-Wall", "-Wextra", *extra,
+           "-o", tmp] + _SOURCES + ["-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, path)
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle into ``oracle/_build/liboracle.so`` (plain gcc, -O2)."""
-    if force or _stale():
-        os.makedirs(_BUILD_DIR, exist_ok=True)
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-Wall", "-Wextra",
-               "-o", tmp] + _SOURCES + ["-lm"]
-        subprocess.run(cmd, check=True)
-        os.replace(tmp, _LIB_PATH)
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (plain gcc, -O2),
+    and, where gcc supports OpenMP, the same source with the row loops split
+    over the host's cores into ``liboracle_omp.so`` (used only to time the
+    CPU baseline on all cores)."""
+    if force or _stale_lib(_LIB_PATH):
+        _compile(_LIB_PATH, ["-Wno-unknown-pragmas"])
+    if force or _stale_lib(_OMP_LIB_PATH):
+        try:
+            _compile(_OMP_LIB_PATH, ["-fopenmp"])
+        except (subprocess.CalledProcessError, OSError):
+            pass
     return _LIB_PATH
+
+
+def has_all_cores() -> bool:
+    """True when the OpenMP build of the oracle exists."""
+    build()
+    return os.path.exists(_OMP_LIB_PATH)
+
+
+def use_all_cores(on: bool) -> None:
+    """Route every following oracle call to the OpenMP build (on=True) or the
+    plain single-threaded build (on=False, the default)."""
+    global _lib, _use_omp
+    with _lock:
+        if on != _use_omp:
+            _use_omp = on
+            _lib = None
+
+
+_use_omp = False
 
 
 def _load():
@@ -56,7 +90,7 @@ def _load():
     with _lock:
         if _lib is None:
             build()
-            lib = ctypes.CDLL(_LIB_PATH)
+            lib = ctypes.CDLL(_OMP_LIB_PATH if _use_omp and os.path.exists(_OMP_LIB_PATH) else _LIB_PATH)
             P = ctypes.c_void_p
             I64 = ctypes.c_int64
             I = ctypes.c_int

@@ -7,6 +7,11 @@
  */
 #include "pti_oracle.h"
 
+/* The row (and verify-step) loops carry "#pragma omp parallel for": built
+ * with -fopenmp (the CPU-baseline timing of the benchmark) the rows are split
+ * over the host's cores, each row still computed by the same loop; built
+ * without it (the tests) the pragmas are ignored.  Rows are independent, so
+ * the results are identical either way. */
 #include <math.h>
 #include <stddef.h>
 #include <stdlib.h>
@@ -169,6 +174,7 @@ int pti_or_q8_gemv_rows(const uint8_t *w, int64_t rows, int64_t cols, int n,
 
     for (s = 0; s < n; ++s) {
         const float *xs = x + (int64_t)s * cols;
+#pragma omp parallel for private(k) schedule(static)
         for (j = 0; j < n_idx; ++j) {
             double acc = 0.0, mag = 0.0;
             for (k = 0; k < cols; ++k) {
@@ -205,6 +211,7 @@ int pti_or_twin_gemv_rows(const uint8_t *w, int64_t rows, int64_t cols,
         if (rows_idx[j] < 0 || rows_idx[j] >= rows)
             return -1;
 
+#pragma omp parallel for private(k) schedule(static)
     for (j = 0; j < n_idx; ++j) {
         double acc_a = 0.0, acc_b = 0.0, mag_a = 0.0, mag_b = 0.0;
         for (k = 0; k < cols; ++k) {
@@ -244,6 +251,7 @@ int pti_or_verify_greedy(const float *logits, const int32_t *guess, int64_t step
     if (steps < 0 || n < 1 || vocab < 1 || (n > 1 && match == NULL))
         return -1;
 
+#pragma omp parallel for private(s, v) schedule(static)
     for (t = 0; t < steps; ++t) {
         int run = 1;
         int32_t accepted = 0;
@@ -364,6 +372,7 @@ int pti_or_verify_sample(const float *logits, const int32_t *guess, const float 
 static void q8_matvec_f64(const uint8_t *w, int64_t rows, int64_t cols, const double *x, double *y)
 {
     int64_t r, k;
+#pragma omp parallel for private(k) schedule(static)
     for (r = 0; r < rows; ++r) {
         double acc = 0.0;
         for (k = 0; k < cols; ++k)

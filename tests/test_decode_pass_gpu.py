@@ -161,7 +161,9 @@ def test_decode_pass_64_layers(capsys):
     """64 chained layers at a small size, every layer within its bar.  The
     drift of the whole chain against the oracle's own 64-layer chain is
     printed, not gated: rounding differences are amplified from layer to layer
-    by the random layers themselves, whatever the kernels do."""
+    by the random layers themselves, whatever the kernels do
+    (tests/test_drift_pins.py: the oracle's chain moved by one fp32 ulp at its
+    input diverges to max |diff| of order one over the same 64 layers)."""
     hidden, ffn, n = 256, 512, 4
     layers = host_layers(64, hidden, ffn, seed=21)
     x = pti_synth.activations(n, hidden, 21, 1000)

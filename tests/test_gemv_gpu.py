@@ -5,6 +5,8 @@ oracle's exact bound.  Special cases whose result is exact in fp32 (one-hot x,
 integer weights and activations, zero weights, identical twins) are checked
 bit for bit.  Inputs come from the seeded generator (pti_synth) only.
 """
+import contextlib
+
 import numpy as np
 import pytest
 import torch
@@ -37,6 +39,17 @@ def assert_parity(y_gpu, y_ref, bound, what=""):
     if bad.any():
         ratio = np.max(err / np.maximum(bound, 1e-300))
         raise AssertionError(f"{what}: {bad.sum()} outputs off, max err/bound {ratio:.3g}")
+
+
+@contextlib.contextmanager
+def all_cores():
+    """The oracle's OpenMP build for the full-size checks (rows are independent,
+    so its results equal the single-threaded build's bit for bit)."""
+    oracle.use_all_cores(True)
+    try:
+        yield
+    finally:
+        oracle.use_all_cores(False)
 
 
 def tile_sample_rows(rows, rng):
@@ -127,17 +140,16 @@ def full_q8():
 
 
 @pytest.mark.parametrize("rows,cols", [(17408, 5120), (5120, 17408)])
-def test_q8_full_size_matches_oracle_on_every_tile(full_q8, rows, cols):
+def test_q8_full_size_matches_oracle_on_every_row(full_q8, rows, cols):
     w_np = full_q8[(rows, cols)]
     w = dev(w_np)
-    rng = np.random.default_rng(rows)
-    idx = tile_sample_rows(rows, rng)
     for n in (1, 2, 3, 4):
         x = pti_synth.activations(n, cols, seed=0, tensor_id=100 + n)
         y = pti.q8_gemv_nstream(w, rows, cols, dev(x)).cpu().numpy()
         assert np.isfinite(y).all()
-        y_ref, bound = oracle.q8_gemv(w_np, rows, cols, x, rows_idx=idx)
-        assert_parity(y[:, idx], y_ref, bound, f"q8 {rows}x{cols} n={n}")
+        with all_cores():
+            y_ref, bound = oracle.q8_gemv(w_np, rows, cols, x)
+        assert_parity(y, y_ref, bound, f"q8 {rows}x{cols} n={n}")
 
 
 def test_q8_streams_are_independent_at_full_size(full_q8):
@@ -218,14 +230,14 @@ def full_twin():
 
 
 @pytest.mark.parametrize("rows,cols", [(17408, 5120), (5120, 17408)])
-def test_twin_full_size_matches_oracle_on_every_tile(full_twin, rows, cols):
+def test_twin_full_size_matches_oracle_on_every_row(full_twin, rows, cols):
     w_np = full_twin[(rows, cols)]
     xa, xb = pti_synth.activations(2, cols, seed=0, tensor_id=200)
     ya, yb = pti.ssq_twin_gemv(dev(w_np), rows, cols, dev(xa), dev(xb))
-    idx = tile_sample_rows(rows, np.random.default_rng(rows + 1))
-    ya_ref, yb_ref, ba, bb = oracle.twin_gemv(w_np, rows, cols, xa, xb, rows_idx=idx)
-    assert_parity(ya.cpu().numpy()[idx], ya_ref, ba, "twin A full")
-    assert_parity(yb.cpu().numpy()[idx], yb_ref, bb, "twin B full")
+    with all_cores():
+        ya_ref, yb_ref, ba, bb = oracle.twin_gemv(w_np, rows, cols, xa, xb)
+    assert_parity(ya.cpu().numpy(), ya_ref, ba, "twin A full")
+    assert_parity(yb.cpu().numpy(), yb_ref, bb, "twin B full")
 
 
 def test_twin_pdl_chain_reads_each_finished_output(full_twin):
@@ -274,18 +286,19 @@ def test_twin_nstream_matches_oracle(rows, cols, n):
 @pytest.mark.parametrize("rows,cols", [(17408, 5120), (5120, 17408)])
 def test_twin_two_streams_per_model_full_size(full_twin, rows, cols):
     """Four tokens per weight load: two streams of each twin at full size,
-    every row tile sampled; stream 0 equals the one-stream call within the bar."""
+    every row checked; stream 0 equals the one-stream call within the bar."""
     w_np = full_twin[(rows, cols)]
     w = dev(w_np)
     xa = pti_synth.activations(2, cols, seed=0, tensor_id=400)
     xb = pti_synth.activations(2, cols, seed=0, tensor_id=401)
     ya, yb = pti.ssq_twin_gemv_nstream(w, rows, cols, dev(xa), dev(xb))
     ya, yb = ya.cpu().numpy(), yb.cpu().numpy()
-    idx = tile_sample_rows(rows, np.random.default_rng(rows + 2))
     for s in range(2):
-        ra, rb, ba, bb = oracle.twin_gemv(w_np, rows, cols, xa[s], xb[s], rows_idx=idx)
-        assert_parity(ya[s, idx], ra, ba, f"A stream {s}")
-        assert_parity(yb[s, idx], rb, bb, f"B stream {s}")
+        with all_cores():
+            ra, rb, ba, bb = oracle.twin_gemv(w_np, rows, cols, xa[s], xb[s])
+        assert_parity(ya[s], ra, ba, f"A stream {s}")
+        assert_parity(yb[s], rb, bb, f"B stream {s}")
+    idx = tile_sample_rows(rows, np.random.default_rng(rows + 2))
     y1a, y1b = pti.ssq_twin_gemv(w, rows, cols, dev(xa[0]), dev(xb[0]))
     _, _, ba, bb = oracle.twin_gemv(w_np, rows, cols, xa[0], xb[0], rows_idx=idx)
     assert np.all(np.abs(ya[0, idx].astype(np.float64) - y1a.cpu().numpy()[idx]) <= 2 * TOL * ba)
