@@ -175,12 +175,13 @@ class Q8Pass:
     """N-stream Q8 GEMV over L distinct rows x cols matrices (one step = one pass)."""
     sources = GEMV_SOURCES
 
-    def __init__(self, rows=17408, cols=5120, n=4, layers=16, seed=0, w=None):
+    def __init__(self, rows=17408, cols=5120, n=4, layers=16, seed=0, w=None, flags=0):
         import torch
         import pti_synth
         import stream_quantized_gemv_gb300 as pti
         self.pti, self.torch = pti, torch
         self.rows, self.cols, self.n, self.layers = rows, cols, n, layers
+        self.flags = flags  # FLAG_TENSOR_CORES: the tensor-core consumer
         self.name = f"q8_gemv_n{n}_{rows}x{cols}_x{layers}"
         self.w = w if w is not None else [pti_synth.q8_matrix_device(rows, cols, seed, 1000 + i)
                                           for i in range(layers)]
@@ -208,7 +209,7 @@ class Q8Pass:
         y = self.y if y is None else y
         for k, w in enumerate(self.w):
             self.pti.q8_gemv_nstream(w, self.rows, self.cols, x, y=y, ws=self.ws,
-                                     flags=self.pti.FLAG_PDL if k > 0 else 0)
+                                     flags=(self.pti.FLAG_PDL if k > 0 else 0) | self.flags)
 
     def e2e_buffers(self):
         t = self.torch
@@ -678,17 +679,19 @@ def q8_target(a, world, local, peak, peak_kind):
     same harness (16 distinct matrices per step, launches after the first
     chained by programmatic dependent launch, CUDA-graph replay): time per
     GEMV, effective GB/s, fractions of the measured and the nominal HBM rate,
-    and the step-time ratio N=4 / N=1."""
+    and the step-time ratio N=4 / N=1; also N=4 with the products on the
+    tensor core (the opt-in consumer) for comparison."""
     import torch
+    import stream_quantized_gemv_gb300 as pti
     out = {"shape": "17408x5120", "matrices_per_step": 16, "steps": a.steps}
     shared = None
-    for n in (1, 4):
-        wl = Q8Pass(17408, 5120, n, 16, w=shared)
+    for n, key, flags in ((1, "n1", 0), (4, "n4", 0), (4, "n4_tensor_cores", pti.FLAG_TENSOR_CORES)):
+        wl = Q8Pass(17408, 5120, n, 16, w=shared, flags=flags)
         shared = wl.w
         ms, clocks = time_gpu(wl, a.steps, a.warmup, world, local)
         us = ms * 1e3 / wl.layers
         gbs = wl.launch_bytes / (us * 1e-6) / 1e9
-        out[f"n{n}"] = {"us_per_gemv": round(us, 3), "gbs": round(gbs, 1),
+        out[key] = {"us_per_gemv": round(us, 3), "gbs": round(gbs, 1),
                         "of_measured": round(gbs / peak, 4), "of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
                         "stream_tokens_per_s": round(n / (us * 1e-6), 1), "clocks": clocks}
         del wl

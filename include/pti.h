@@ -105,7 +105,12 @@ const char *pti_status_string(pti_status status);
  * adds the partial sums of the row tiles several CTAs shared (launched with
  * programmatic dependent launch, so it waits for the GEMV without a launch
  * gap); other calls use a plain per-row kernel with the same bound on the
- * error (a different rounding order).
+ * error (a different rounding order).  The fast path forms the products on
+ * the CUDA cores (exact dequantisation, fp32 FMAs); with PTI_FLAG_TENSOR_CORES
+ * (the _ex variant) on the tensor core instead (tcgen05.mma on binary16
+ * operands that hold every weight and, split into three pieces, every fp32
+ * activation exactly, with fp32 accumulation): same error bound, measured
+ * no faster on GB300.
  */
 size_t pti_q8_gemv_workspace_bytes(int64_t rows, int64_t cols, int n_streams);
 
@@ -125,9 +130,16 @@ pti_status pti_q8_gemv_nstream(const void *w_q8, int64_t rows, int64_t cols, int
  *                 promises that the preceding work in the stream does not write
  *                 the weights.  This hides most of the launch and ramp-up time
  *                 of a GEMV that follows another kernel (a decode step's chain
- *                 of GEMVs).  Other flag bits return PTI_ERR_VALUE.
+ *                 of GEMVs).
+ *   PTI_FLAG_CUDA_CORES, PTI_FLAG_TENSOR_CORES  (Q8 GEMV only) the fast
+ *                 path's products on the CUDA cores (the default) or on the
+ *                 tensor core; both at once return PTI_ERR_VALUE, and so does
+ *                 either one on the twin GEMVs.
+ * Other flag bits return PTI_ERR_VALUE.
  */
 #define PTI_FLAG_PDL 0x1u
+#define PTI_FLAG_CUDA_CORES 0x2u
+#define PTI_FLAG_TENSOR_CORES 0x4u
 
 pti_status pti_q8_gemv_nstream_ex(const void *w_q8, int64_t rows, int64_t cols, int n_streams,
                                   const float *x, float *y,
@@ -418,11 +430,13 @@ pti_status pti_selfspec_greedy(const pti_toy_model *model, int n_streams, int32_
  *               count (units / grid, units = (rows/128 rounded up) (cols/256),
  *               grid = min(SM count, units, 320)); else PTI_ERR_VALUE.
  *   wait_ns     1000 .. 2e9; else PTI_ERR_VALUE.
+ *   flags       0, PTI_FLAG_CUDA_CORES or PTI_FLAG_TENSOR_CORES (which
+ *               consumer runs, as for pti_q8_gemv_nstream_ex).
  * Other arguments and checks as pti_q8_gemv_nstream.
  */
 pti_status pti_test_q8_gemv_stall(const void *w_q8, int64_t rows, int64_t cols, int n_streams,
                                   const float *x, float *y, void *workspace, size_t workspace_bytes,
-                                  pti_stream_t stream, int64_t stall_unit, uint64_t wait_ns);
+                                  pti_stream_t stream, int64_t stall_unit, uint64_t wait_ns, uint32_t flags);
 
 /*
  * Reads and clears the device error word of the current device (a blocking

@@ -96,7 +96,8 @@ def lib() -> ctypes.CDLL:
             L.pti_selfspec_greedy.restype = I
             L.pti_selfspec_greedy.argtypes = [ctypes.POINTER(ToyModel), I, ctypes.c_int32, I, P, I64, P, P, P, SZ, P]
             L.pti_test_q8_gemv_stall.restype = I
-            L.pti_test_q8_gemv_stall.argtypes = [P, I64, I64, I, P, P, P, SZ, P, I64, ctypes.c_uint64]
+            L.pti_test_q8_gemv_stall.argtypes = [P, I64, I64, I, P, P, P, SZ, P, I64, ctypes.c_uint64,
+                                                 ctypes.c_uint32]
             L.pti_device_error.restype = I
             L.pti_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
             _lib = L
@@ -146,12 +147,16 @@ def ssq_twin_gemv_workspace_bytes(rows: int, cols: int) -> int:
 
 
 FLAG_PDL = 0x1
+FLAG_CUDA_CORES = 0x2
+FLAG_TENSOR_CORES = 0x4
 
 
 def q8_gemv_nstream(w, rows: int, cols: int, x, y=None, ws=None, stream=None, flags: int = 0):
     """y[s] = W x[s] for the n = x.shape[0] streams (1..4).  ``w``: uint8 Q8 bytes.
     ``flags=FLAG_PDL`` lets the kernel start while the previous kernel in the
-    stream runs (that kernel must not write ``w``)."""
+    stream runs (that kernel must not write ``w``); ``FLAG_CUDA_CORES`` or
+    ``FLAG_TENSOR_CORES`` picks the fast path's consumer (default: CUDA
+    cores)."""
     import torch
     if x.dim() == 1:
         x = x.unsqueeze(0)
@@ -346,10 +351,12 @@ def selfspec_greedy(embedding, w_gate, w_up, w_down, w_head, vocab: int, hidden:
     return tokens[:cap], count, accept[:steps]
 
 
-def test_q8_gemv_stall(w, rows: int, cols: int, x, stall_unit: int, wait_ns: int, y=None, ws=None, stream=None):
+def test_q8_gemv_stall(w, rows: int, cols: int, x, stall_unit: int, wait_ns: int, y=None, ws=None, stream=None,
+                      flags: int = 0):
     """The testing hook ``pti_test_q8_gemv_stall``: a fast-path Q8 GEMV whose
     first CTA stops issuing copies at unit ``stall_unit``, with every pipeline
-    wait bounded by ``wait_ns``.  Returns y (undefined after the stall)."""
+    wait bounded by ``wait_ns`` (``flags``: FLAG_CUDA_CORES or
+    FLAG_TENSOR_CORES).  Returns y (undefined after the stall)."""
     import torch
     n = x.shape[0]
     if y is None:
@@ -359,7 +366,7 @@ def test_q8_gemv_stall(w, rows: int, cols: int, x, stall_unit: int, wait_ns: int
         ws = workspace(need, x.device)
     _check(lib().pti_test_q8_gemv_stall(_ptr(w), rows, cols, n, _ptr(x), _ptr(y), _ptr(ws),
                                         0 if ws is None else ws.numel() * ws.element_size(), _stream(stream),
-                                        int(stall_unit), int(wait_ns)), "pti_test_q8_gemv_stall")
+                                        int(stall_unit), int(wait_ns), int(flags)), "pti_test_q8_gemv_stall")
     return y
 
 

@@ -113,9 +113,19 @@ extern "C" size_t pti_ssq_twin_gemv_nstream_workspace_bytes(int64_t rows, int64_
 }
 
 namespace {
+// The consumer a Q8 call's flags ask for (false: an invalid combination).
+bool cores_of_flags(uint32_t flags, Cores *cores) {
+  const uint32_t c = flags & (PTI_FLAG_CUDA_CORES | PTI_FLAG_TENSOR_CORES);
+  if (c == (PTI_FLAG_CUDA_CORES | PTI_FLAG_TENSOR_CORES)) return false;
+  *cores = c == PTI_FLAG_CUDA_CORES ? Cores::Cuda : c == PTI_FLAG_TENSOR_CORES ? Cores::Tensor : Cores::Auto;
+  return true;
+}
+
 pti_status q8_gemv(const void *w_q8, int64_t rows, int64_t cols, int n_streams, const float *x, float *y,
                    void *workspace, size_t workspace_bytes, pti_stream_t stream, uint32_t flags) {
-  if ((flags & ~PTI_FLAG_PDL) != 0u) return PTI_ERR_VALUE;
+  if ((flags & ~(PTI_FLAG_PDL | PTI_FLAG_CUDA_CORES | PTI_FLAG_TENSOR_CORES)) != 0u) return PTI_ERR_VALUE;
+  Cores cores = Cores::Auto;
+  if (!cores_of_flags(flags, &cores)) return PTI_ERR_VALUE;
   const bool pdl = (flags & PTI_FLAG_PDL) != 0u;
   if (w_q8 == nullptr || x == nullptr || y == nullptr) return PTI_ERR_NULL;
   if (const pti_status s = check_gemv_shape(rows, cols); s != PTI_OK) return s;
@@ -136,10 +146,10 @@ pti_status q8_gemv(const void *w_q8, int64_t rows, int64_t cols, int n_streams, 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (need > 0 && aligned(x, 16)) {
     switch (n_streams) {
-      case 1: return launch_fast<Fmt::Q8, 1>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st, pdl);
-      case 2: return launch_fast<Fmt::Q8, 2>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st, pdl);
-      case 3: return launch_fast<Fmt::Q8, 3>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st, pdl);
-      default: return launch_fast<Fmt::Q8, 4>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st, pdl);
+      case 1: return launch_fast<Fmt::Q8, 1>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st, pdl, cores);
+      case 2: return launch_fast<Fmt::Q8, 2>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st, pdl, cores);
+      case 3: return launch_fast<Fmt::Q8, 3>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st, pdl, cores);
+      default: return launch_fast<Fmt::Q8, 4>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, st, pdl, cores);
     }
   }
   switch (n_streams) {
@@ -282,7 +292,11 @@ extern "C" pti_status pti_q8_gemv_nstream_noalloc(const void *w_q8, int64_t rows
 // Testing hook: the fast-path Q8 GEMV with a stalled copy (see pti.h).
 extern "C" pti_status pti_test_q8_gemv_stall(const void *w_q8, int64_t rows, int64_t cols, int n_streams,
                                              const float *x, float *y, void *workspace, size_t workspace_bytes,
-                                             pti_stream_t stream, int64_t stall_unit, uint64_t wait_ns) {
+                                             pti_stream_t stream, int64_t stall_unit, uint64_t wait_ns,
+                                             uint32_t flags) {
+  Cores cores = Cores::Auto;
+  if ((flags & ~(PTI_FLAG_CUDA_CORES | PTI_FLAG_TENSOR_CORES)) != 0u || !cores_of_flags(flags, &cores))
+    return PTI_ERR_VALUE;
   if (w_q8 == nullptr || x == nullptr || y == nullptr || workspace == nullptr) return PTI_ERR_NULL;
   if (const pti_status st = check_gemv_shape(rows, cols); st != PTI_OK) return st;
   if (cols % 256 != 0) return PTI_ERR_SHAPE;
@@ -305,10 +319,14 @@ extern "C" pti_status pti_test_q8_gemv_stall(const void *w_q8, int64_t rows, int
     return PTI_ERR_ALIAS;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (n_streams) {
-    case 1: return launch_fast<Fmt::Q8, 1>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, s, false, wait_ns, stall_unit);
-    case 2: return launch_fast<Fmt::Q8, 2>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, s, false, wait_ns, stall_unit);
-    case 3: return launch_fast<Fmt::Q8, 3>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, s, false, wait_ns, stall_unit);
-    default: return launch_fast<Fmt::Q8, 4>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, s, false, wait_ns, stall_unit);
+    case 1: return launch_fast<Fmt::Q8, 1>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, s, false, cores, wait_ns,
+                                           stall_unit);
+    case 2: return launch_fast<Fmt::Q8, 2>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, s, false, cores, wait_ns,
+                                           stall_unit);
+    case 3: return launch_fast<Fmt::Q8, 3>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, s, false, cores, wait_ns,
+                                           stall_unit);
+    default: return launch_fast<Fmt::Q8, 4>(w_q8, rows, cols, x, nullptr, y, nullptr, workspace, s, false, cores, wait_ns,
+                                             stall_unit);
   }
 }
 

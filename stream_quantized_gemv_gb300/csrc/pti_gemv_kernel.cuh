@@ -549,6 +549,17 @@ __device__ __forceinline__ float warp_total(const float *red, int sl, int s, int
   return tree_sum(v);
 }
 
+// Totals policy of the CUDA-core consumers: kRedWarps parked warp sums per
+// element, 16 consumer warps.
+template <Fmt F>
+struct WarpTotals {
+  static constexpr int kThreads = 16 * 32;
+  template <int kOut>
+  __device__ __forceinline__ static float total(const float *red, int sl, int s, int row) {
+    return warp_total<F, kOut>(red, sl, s, row);
+  }
+};
+
 // Total of element (s, row) of shared tile rb: the partials of its CTAs
 // c_lo .. c_hi added in CTA order, so the result does not depend on which CTA
 // or kernel adds them.  Each CTA's partial sits in slot 0 if rb is its first
@@ -605,20 +616,20 @@ __device__ __forceinline__ void run_epilogue(const GemvArgs &a, float *epi, int3
 }
 
 // Finishes one or two row tiles of the CTA: tile k (row tile rb[k], parked
-// warp sums in red slot sl[k]).  Each element's total is the tree sum of the 8
-// warps that computed it.  A tile no other CTA shares is written out directly
+// sums in red slot sl[k]).  Each element's total is formed from its parked
+// sums by the consumer's totals policy Tot (Tot::kThreads consumer threads).  A tile no other CTA shares is written out directly
 // (Plain) or through the fused epilogue.  A shared tile's totals go to this
 // CTA's partial slot in the workspace, and a separate kernel
 // (combine_tiles_kernel) adds the partials of every shared tile once the GEMV
 // has completed, so a CTA leaves the SM right after its last tile.  Not
 // inlined: it runs a few times per CTA, and one shared copy keeps the consumer
 // loops' instruction footprint small.
-template <Fmt F, int N, Epi E>
+template <Fmt F, int N, Epi E, class Tot>
 __device__ __noinline__ void finish_tiles(const GemvArgs &a, const float *red, int count, int32_t rb0, int sl0,
                                           int32_t rb1, int sl1, uint32_t tid, float *epi) {
   using T = Traits<F, N>;
   constexpr int kOut = T::kOut;
-  constexpr int kConsumerThreads = T::kWarps * 32;
+  constexpr int kConsumerThreads = Tot::kThreads;
   const int32_t rbs[2] = {rb0, rb1};
   const int sls[2] = {sl0, sl1};
   bool epilogue_ran = false;
@@ -629,7 +640,7 @@ __device__ __noinline__ void finish_tiles(const GemvArgs &a, const float *red, i
       for (int t = tid; t < kOut * kRowsPerTile; t += kConsumerThreads) {
         const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
         a.part[((static_cast<int64_t>(blockIdx.x) * 2 + sls[k]) * kOut + s) * kRowsPerTile + row] =
-            warp_total<F, kOut>(red, sls[k], s, row);
+            Tot::template total<kOut>(red, sls[k], s, row);
       }
       continue;
     }
@@ -637,7 +648,7 @@ __device__ __noinline__ void finish_tiles(const GemvArgs &a, const float *red, i
       if (epilogue_ran) named_barrier(kBarConsumers, kConsumerThreads);  // tile_out and wsum are reused
     for (int t = tid; t < kOut * kRowsPerTile; t += kConsumerThreads) {
       const int s = t / kRowsPerTile, row = t - s * kRowsPerTile;
-      deliver<F, N, E>(a, epi, rbs[k], s, row, warp_total<F, kOut>(red, sls[k], s, row));
+      deliver<F, N, E>(a, epi, rbs[k], s, row, Tot::template total<kOut>(red, sls[k], s, row));
     }
     if constexpr (E != Epi::Plain) {
       named_barrier(kBarConsumers, kConsumerThreads);
@@ -696,6 +707,25 @@ struct ConsumerCtx {
   int64_t u0, u1;           // this CTA's unit range
 };
 
+// Fused epilogues: consumer warp s < kOut derives the RMS scale of input
+// vector s from the per-tile sums of squares that the producer staged in
+// shared memory (or, when they were too many to stage, from global memory
+// after the wait on the previous kernel); CTA 0 also hands the scales to the
+// tile-combine kernel.
+template <int kOut>
+__device__ __forceinline__ void derive_input_scale(const GemvArgs &a, const ConsumerCtx &c, uint64_t limit) {
+  const bool staged = staged_sum_bytes<kOut>(a) != 0u;
+  if (staged && !mbar_try_wait(c.sq_bar, 0) && !mbar_wait_bounded(c.sq_bar, 0, c.flags, limit)) {
+    if (c.flag[0] == 0) atomicOr(&g_device_error, PTI_DEVERR_FULL_TIMEOUT);
+    c.flag[0] = 1;
+    return;
+  }
+  if (!staged && a.sq_in != nullptr) pdl_wait_primary();  // the sums come from the previous kernel
+  float *const scale = c.epi + 4 * kRowsPerTile;
+  input_scale_of_stream<kOut>(a, staged ? c.sq_stage : 0u, c.warp, c.lane, scale);
+  if (c.lane == 0 && blockIdx.x == 0 && a.scale_out != nullptr) a.scale_out[c.warp] = scale[c.warp];
+}
+
 // The consumer warps' walk over the CTA's units: wait for each stage, run the
 // consumer `cons` on it (the warp's share of the unit), release the stage; at
 // the end of each row tile park the warp's sums, and finish the tiles.
@@ -718,16 +748,7 @@ __device__ __forceinline__ void consumer_loop(const GemvArgs &a, const ConsumerC
   auto wait_scales = [&]() {
     if (scales_ready) return;
     scales_ready = true;
-    const bool staged = staged_sum_bytes<kOut>(a) != 0u;
-    if (staged && !mbar_try_wait(c.sq_bar, 0) && !mbar_wait_bounded(c.sq_bar, 0, c.flags, limit)) {
-      if (c.flag[0] == 0) atomicOr(&g_device_error, PTI_DEVERR_FULL_TIMEOUT);
-      c.flag[0] = 1;
-      return;
-    }
-    if (!staged && a.sq_in != nullptr) pdl_wait_primary();  // the sums come from the previous kernel
-    float *const scale = c.epi + 4 * kRowsPerTile;
-    input_scale_of_stream<kOut>(a, staged ? c.sq_stage : 0u, c.warp, c.lane, scale);
-    if (c.lane == 0 && blockIdx.x == 0 && a.scale_out != nullptr) a.scale_out[c.warp] = scale[c.warp];
+    derive_input_scale<kOut>(a, c, limit);
   };
   const int32_t rb_first = static_cast<int32_t>(c.u0 / a.n_sb);
   const int32_t rb_last = static_cast<int32_t>((c.u1 - 1) / a.n_sb);
@@ -767,13 +788,14 @@ __device__ __forceinline__ void consumer_loop(const GemvArgs &a, const ConsumerC
       // pass do: 20 units per tile, about 36 per CTA)
       wait_scales();
       named_barrier(kBarConsumers, kConsumerThreads);
-      finish_tiles<F, N, E>(a, c.red, 1, rb, 1, 0, 0, c.tid, c.epi);
+      finish_tiles<F, N, E, WarpTotals<F>>(a, c.red, 1, rb, 1, 0, 0, c.tid, c.epi);
       named_barrier(kBarConsumers, kConsumerThreads);
     }
   }
   wait_scales();
   named_barrier(kBarConsumers, kConsumerThreads);
-  finish_tiles<F, N, E>(a, c.red, rb_last != rb_first ? 2 : 1, rb_first, 0, rb_last, 1, c.tid, c.epi);
+  finish_tiles<F, N, E, WarpTotals<F>>(a, c.red, rb_last != rb_first ? 2 : 1, rb_first, 0, rb_last, 1, c.tid,
+                                       c.epi);
 }
 
 // The copy side of the ring, run by lane 0 of the producer warp: it fills the
@@ -793,6 +815,7 @@ struct Producer {
   int64_t u0, nu, issued;
   uint64_t pol;
   uint32_t sq_bar, sq_stage;  // fused epilogues: barrier and buffer of the staged input sums
+  int32_t ramp;               // initial stages in flight before the next waits for its predecessor
   // Row tile and super-block of the next unit whose weights (w) and
   // activations (x) are to be fetched.  Copies are issued in unit order, so
   // both cursors only step forward (no division per unit: the producer warp
@@ -839,18 +862,18 @@ struct Producer {
   }
   // Weights do not depend on the previous kernel in the stream: fetch the
   // first tiles before waiting for it, then their activations.  When the
-  // consumers are the slower side (Q8 with N >= 2), only `ramp` stages go out
-  // at once and each further initial stage waits until the one `ramp` before
-  // it has landed: with every SM requesting its whole ring at the same moment
-  // the first stage would otherwise land only after most of the burst
-  // (measured: about 4 us), and compute could not start before.  Chained
-  // decode-pass launches (prefetch_all) fetch every initial stage before the
-  // wait: the previous kernel's tile combine leaves time for all of them.
+  // consumers are the slower side (the CUDA-core Q8 consumer with N >= 2),
+  // the kernel sets `ramp` to 2: only that many stages go out at once and
+  // each further initial stage waits until the one `ramp` before it has
+  // landed; with every SM requesting its whole ring at the same moment the
+  // first stage would otherwise land only after most of the burst (measured:
+  // about 4 us), and compute could not start before.  Chained decode-pass
+  // launches (prefetch_all) fetch every initial stage before the wait: the
+  // previous kernel's tile combine leaves time for all of them.
   __device__ __forceinline__ void start() {
     prefetch_tmap(tmap);
     if constexpr (E == Epi::GateUp) prefetch_tmap(tmap2);
     init_cursors();
-    const int64_t ramp = (F == Fmt::Q8 && N >= 2 && !a->prefetch_all) ? 2 : kMaxStages;
     const int64_t pre = nu < stages ? nu : stages;
     const int64_t first = pre < ramp ? pre : ramp;
     for (int64_t i = 0; i < first; ++i) {
@@ -953,8 +976,9 @@ __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
   if (warp == kConsumerWarps) {
     // ---------------- producer: one lane issues every copy --------------------
     if (lane == 0) {
+      const int32_t ramp = (F == Fmt::Q8 && N >= 2 && !a.prefetch_all) ? 2 : kMaxStages;
       Producer<F, N, E> prod{&tmap, &tmap2, &a, base, bars, flags, flag, stages, u0, u1 - u0, 0,
-                             l2_policy_evict_first(), sq_bar, sq_stage, 0, 0, 0};
+                             l2_policy_evict_first(), sq_bar, sq_stage, ramp, 0, 0, 0};
       prod.start();
       uint32_t st = 0, ph = 0;
       for (int64_t i = 0; i + stages < prod.nu && flag[0] == 0; ++i) {
@@ -995,6 +1019,9 @@ __global__ void __launch_bounds__(Traits<F, N>::kWarps * 32 + 32, 1)
     }
   }
 }
+
+// The tensor-core consumer of the Q8 kernel (gemv_tc_kernel).
+#include "pti_gemv_tc.cuh"
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -1042,6 +1069,28 @@ TilePlan plan_tiles(int64_t rows, int64_t cols, int sms) {
   return p;
 }
 
+// The same tiling for the tensor-core kernel, with its shared-memory layout.
+template <int N, Epi E>
+TilePlan plan_tiles_tc(int64_t rows, int64_t cols, int sms) {
+  using S = Stage<Fmt::Q8, N>;
+  TilePlan p = plan_tiles<Fmt::Q8, N, E>(rows, cols, sms);
+  const int64_t fixed = 1024 + 2 * kTcBBytes + TcLayout<N>::kXinvBytes + TcLayout<N>::kRedBytes +
+                        8 * (2 * kMaxStages + 4) + 16 + (E == Epi::Plain ? 0 : kEpiBytes + kSqStageBytes);
+  p.stages = static_cast<int32_t>(std::min<int64_t>(kMaxStages, (kSmemOptin - fixed) / S::kBytes));
+  p.smem = static_cast<size_t>(fixed) + static_cast<size_t>(p.stages) * S::kBytes;
+  return p;
+}
+
+// Which consumer a Q8 launch uses: the CUDA-core one (the default: it
+// measured at least as fast at every stream count) or, on request, the
+// tensor-core one.
+enum class Cores : int { Auto = 0, Cuda = 1, Tensor = 2 };
+
+template <Fmt F, int N, Epi E>
+constexpr bool use_tensor_cores(Cores c) {
+  return F == Fmt::Q8 && E == Epi::Plain && c == Cores::Tensor;
+}
+
 // Stream-K partials of one call: [kMaxGrid][2 slots][kout][128] floats.
 inline size_t partial_bytes(int kout) {
   return static_cast<size_t>(kMaxGrid) * 2 * kout * kRowsPerTile * sizeof(float);
@@ -1078,23 +1127,31 @@ bool encode_weight_map(CUtensorMap *tmap, const void *w, int64_t rows, int64_t c
 // (programmatic dependent launch); the kernel reads only weights before it
 // waits for that kernel to complete.
 template <Fmt F, int N, Epi E = Epi::Plain>
-pti_status launch_gemv(const void *w, const void *w2, GemvArgs a, cudaStream_t stream, bool pdl) {
+pti_status launch_gemv(const void *w, const void *w2, GemvArgs a, cudaStream_t stream, bool pdl,
+                       Cores cores = Cores::Auto) {
   using T = Traits<F, N>;
+  constexpr bool kTcCapable = F == Fmt::Q8 && E == Epi::Plain;  // the decode pass runs on the CUDA cores
+  const bool tc = use_tensor_cores<F, N, E>(cores);
   int dev = 0;
   const int sms = current_device_sms(&dev);
   if (sms <= 0) return PTI_ERR_CUDA;
-  const TilePlan p = plan_tiles<F, N, E>(a.rows, a.cols, sms);
+  TilePlan p;
+  if constexpr (kTcCapable) p = tc ? plan_tiles_tc<N, E>(a.rows, a.cols, sms) : plan_tiles<F, N, E>(a.rows, a.cols, sms);
+  else p = plan_tiles<F, N, E>(a.rows, a.cols, sms);
   if (p.stages < 2 || p.smem > static_cast<size_t>(kSmemOptin)) return PTI_ERR_SHAPE;
 
   static std::mutex mu;
-  static bool attr_done[128] = {};
+  static bool attr_done[2][128] = {};
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (!attr_done[dev]) {
-      if (cudaFuncSetAttribute(gemv_tma_kernel<F, N, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemOptin) != cudaSuccess)
-        return launch_status();
-      attr_done[dev] = true;
+    if (!attr_done[tc][dev]) {
+      cudaError_t e = cudaSuccess;
+      if constexpr (kTcCapable) {
+        if (tc) e = cudaFuncSetAttribute(gemv_tc_kernel<N, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOptin);
+      }
+      if (!tc) e = cudaFuncSetAttribute(gemv_tma_kernel<F, N, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOptin);
+      if (e != cudaSuccess) return launch_status();
+      attr_done[tc][dev] = true;
     }
   }
 
@@ -1114,7 +1171,7 @@ pti_status launch_gemv(const void *w, const void *w2, GemvArgs a, cudaStream_t s
   a.stages = p.stages;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
-  cfg.blockDim = dim3(T::kWarps * 32 + 32);
+  cfg.blockDim = dim3(tc ? kTcThreads + 64 : T::kWarps * 32 + 32);
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1122,7 +1179,12 @@ pti_status launch_gemv(const void *w, const void *w2, GemvArgs a, cudaStream_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, gemv_tma_kernel<F, N, E>, tmap, tmap2, a) != cudaSuccess) return launch_status();
+  cudaError_t le = cudaSuccess;
+  if constexpr (kTcCapable) {
+    if (tc) le = cudaLaunchKernelEx(&cfg, gemv_tc_kernel<N, E>, tmap, tmap2, a);
+  }
+  if (!tc) le = cudaLaunchKernelEx(&cfg, gemv_tma_kernel<F, N, E>, tmap, tmap2, a);
+  if (le != cudaSuccess) return launch_status();
   // the shared tiles' partials, once the GEMV has completed (only if a tile
   // spans several CTAs: never when every CTA owns whole tiles)
   if (p.grid > 1) {
@@ -1141,7 +1203,7 @@ pti_status launch_gemv(const void *w, const void *w2, GemvArgs a, cudaStream_t s
 template <Fmt F, int N>
 pti_status launch_fast(const void *w, int64_t rows, int64_t cols, const float *x0, const float *x1,
                        float *y0, float *y1, void *workspace, cudaStream_t stream, bool pdl = false,
-                       uint64_t wait_ns = 0, int64_t stall_unit = -1) {
+                       Cores cores = Cores::Auto, uint64_t wait_ns = 0, int64_t stall_unit = -1) {
   GemvArgs a = {};
   a.wait_ns = wait_ns;
   a.stall_unit = stall_unit;
@@ -1152,7 +1214,7 @@ pti_status launch_fast(const void *w, int64_t rows, int64_t cols, const float *x
   a.part = static_cast<float *>(workspace);
   a.rows = rows;
   a.cols = cols;
-  return launch_gemv<F, N, Epi::Plain>(w, nullptr, a, stream, pdl);
+  return launch_gemv<F, N, Epi::Plain>(w, nullptr, a, stream, pdl, cores);
 }
 
 pti_status check_gemv_shape(int64_t rows, int64_t cols) {

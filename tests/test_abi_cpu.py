@@ -178,12 +178,18 @@ def test_decode_pass_validation(L):
 def test_ex_entry_points_reject_unknown_flags(L):
     """The _ex variants validate like the plain ones and reject unknown flag bits."""
     args = (FAKE, 128, 512, 2, FAKE + (1 << 30), FAKE + (2 << 30), FAKE + (3 << 30), 1 << 24, None)
-    assert L.pti_q8_gemv_nstream_ex(*args, 2) == 8 and L.pti_q8_gemv_nstream_ex(*args, 0x80000000) == 8
+    assert L.pti_q8_gemv_nstream_ex(*args, 8) == 8 and L.pti_q8_gemv_nstream_ex(*args, 0x80000000) == 8
+    # the two consumer choices exclude each other
+    assert L.pti_q8_gemv_nstream_ex(*args, pti.FLAG_CUDA_CORES | pti.FLAG_TENSOR_CORES) == 8
+    assert L.pti_q8_gemv_nstream_ex(None, *args[1:], pti.FLAG_TENSOR_CORES) == 1
     assert L.pti_q8_gemv_nstream_ex(None, *args[1:], 1) == 1
     assert L.pti_q8_gemv_nstream_ex(FAKE, 128, 48, *args[3:], 1) == 2
     targs = (FAKE, 128, 512, FAKE + (1 << 30), FAKE + (1 << 30), FAKE + (2 << 30), FAKE + (2 << 30) + 4096,
              FAKE + (3 << 30), 1 << 24, None)
-    assert L.pti_ssq_twin_gemv_ex(*targs, 4) == 8
+    assert L.pti_ssq_twin_gemv_ex(*targs, 8) == 8
+    # the twin GEMV has one consumer: the core choice is a Q8 flag
+    assert L.pti_ssq_twin_gemv_ex(*targs, pti.FLAG_CUDA_CORES) == 8
+    assert L.pti_ssq_twin_gemv_ex(*targs, pti.FLAG_TENSOR_CORES) == 8
     assert L.pti_ssq_twin_gemv_ex(None, *targs[1:], 1) == 1
 
 
@@ -199,8 +205,8 @@ def test_stall_hook_validation(L):
     """The testing hook checks its arguments like the GEMV (nothing launched)."""
     x, y, ws = FAKE + (1 << 30), FAKE + (2 << 30), FAKE + (3 << 30)
 
-    def call(w=FAKE, rows=1024, cols=512, n=2, x=x, y=y, ws=ws, ws_bytes=1 << 24, stall=8, wait=10 ** 6):
-        return L.pti_test_q8_gemv_stall(w, rows, cols, n, x, y, ws, ws_bytes, None, stall, wait)
+    def call(w=FAKE, rows=1024, cols=512, n=2, x=x, y=y, ws=ws, ws_bytes=1 << 24, stall=8, wait=10 ** 6, flags=0):
+        return L.pti_test_q8_gemv_stall(w, rows, cols, n, x, y, ws, ws_bytes, None, stall, wait, flags)
 
     assert call(w=None) == 1 and call(ws=None) == 1
     assert call(cols=96) == 2 and call(cols=128) == 2           # the hook needs the fast path
@@ -208,6 +214,7 @@ def test_stall_hook_validation(L):
     assert call(x=x + 4) == 4 and call(ws=ws + 16) == 4
     assert call(ws_bytes=256) == 7
     assert call(wait=999) == 8 and call(wait=3 * 10 ** 9) == 8
+    assert call(flags=pti.FLAG_CUDA_CORES | pti.FLAG_TENSOR_CORES) == 8 and call(flags=pti.FLAG_PDL) == 8
 
 
 def test_twin_nstream_validation(L):

@@ -187,6 +187,91 @@ def test_q8_pdl_chain_reads_each_finished_output(full_q8):
 
 
 # ---------------------------------------------------------------------------
+# Q8 on the tensor core (PTI_FLAG_TENSOR_CORES): the same bar
+# ---------------------------------------------------------------------------
+TC = pti.FLAG_TENSOR_CORES
+TC_SHAPES = [(256, 512), (1, 256), (33, 256), (200, 768), (129, 1024), (1000, 2048), (4096, 5120)]
+
+
+@pytest.mark.parametrize("rows,cols", TC_SHAPES)
+@pytest.mark.parametrize("n", [1, 2, 3, 4])
+def test_tc_small_shapes_match_oracle(rows, cols, n):
+    w = pti_synth.q8_matrix(rows, cols, seed=rows * 5 + cols, tensor_id=n)
+    x = pti_synth.activations(n, cols, seed=rows + 3 * cols, tensor_id=n)
+    y_ref, bound = oracle.q8_gemv(w, rows, cols, x)
+    y = pti.q8_gemv_nstream(dev(w), rows, cols, dev(x), flags=TC).cpu().numpy()
+    assert_parity(y, y_ref, bound, f"tc {rows}x{cols} n={n}")
+
+
+def test_tc_exact_cases():
+    """One-hot x, integer x with unit scales, extreme bytes: results exact in
+    fp32 on the tensor core too (every product and partial sum is)."""
+    rows, cols = 300, 512
+    w = pti_synth.q8_matrix(rows, cols, seed=5)
+    for j in (0, 1, 31, 32, 255, 256, 511):
+        x = np.zeros((4, cols), np.float32)
+        x[0, j], x[1, (j + 1) % cols], x[2, j], x[3, (j + 100) % cols] = 1.0, -1.0, 2.0, 0.5
+        y_ref, _ = oracle.q8_gemv(w, rows, cols, x)
+        y = pti.q8_gemv_nstream(dev(w), rows, cols, dev(x), flags=TC).cpu().numpy().astype(np.float64)
+        assert np.array_equal(y, y_ref), j
+    rows, cols = 257, 1024
+    wi = pti_synth.q8_matrix(rows, cols, seed=9).reshape(-1, 34).copy()
+    wi[:, 0], wi[:, 1] = 0x00, 0x3C
+    wi[0::5, 2:] = 0x80
+    wi[1::5, 2:] = 0x7F
+    wi = wi.reshape(-1)
+    xi = np.random.default_rng(2).integers(-4, 5, size=(4, cols)).astype(np.float32)
+    y_ref, _ = oracle.q8_gemv(wi, rows, cols, xi)
+    y = pti.q8_gemv_nstream(dev(wi), rows, cols, dev(xi), flags=TC).cpu().numpy().astype(np.float64)
+    assert np.array_equal(y, y_ref)
+
+
+def test_tc_activation_range():
+    """The activation pieces are scaled per (block, stream): blocks of very
+    different magnitude, spreads of 2^20 inside a block, zeros and
+    subnormals stay within the bar."""
+    rows, cols = 512, 2048
+    w = pti_synth.q8_matrix(rows, cols, seed=11)
+    x = pti_synth.activations(4, cols, seed=11).astype(np.float64)
+    rng = np.random.default_rng(11)
+    x[0] *= np.repeat(2.0 ** rng.integers(-60, 60, cols // 32), 32)    # block magnitudes 2^-60 .. 2^60
+    x[1] *= 2.0 ** rng.integers(-20, 1, cols)                            # spread inside each block
+    x[2, ::3] = 0.0
+    x[2, 1::7] = 1e-40                                                   # fp32 subnormals
+    x[3, :64] = 0.0                                                      # all-zero blocks
+    x = x.astype(np.float32)
+    y_ref, bound = oracle.q8_gemv(w, rows, cols, x)
+    y = pti.q8_gemv_nstream(dev(w), rows, cols, dev(x), flags=TC).cpu().numpy()
+    assert_parity(y, y_ref, bound, "tc activation range")
+
+
+@pytest.mark.parametrize("rows,cols", [(17408, 5120), (5120, 17408)])
+def test_tc_full_size_matches_oracle_on_every_row(full_q8, rows, cols):
+    w_np = full_q8[(rows, cols)]
+    w = dev(w_np)
+    for n in (2, 4):
+        x = pti_synth.activations(n, cols, seed=0, tensor_id=200 + n)
+        y = pti.q8_gemv_nstream(w, rows, cols, dev(x), flags=TC).cpu().numpy()
+        with all_cores():
+            y_ref, bound = oracle.q8_gemv(w_np, rows, cols, x)
+        assert_parity(y, y_ref, bound, f"tc {rows}x{cols} n={n}")
+
+
+def test_tc_pdl_chain_and_bit_reproducible(full_q8):
+    a, b = full_q8[(17408, 5120)], full_q8[(5120, 17408)]
+    wa, wb = dev(a), dev(b)
+    x = dev(pti_synth.activations(4, 5120, seed=19))
+    y1 = pti.q8_gemv_nstream(wa, 17408, 5120, x, flags=TC)
+    y2 = pti.q8_gemv_nstream(wb, 5120, 17408, y1, flags=TC | pti.FLAG_PDL)
+    y2b = pti.q8_gemv_nstream(wb, 5120, 17408, y1, flags=TC | pti.FLAG_PDL)
+    torch.cuda.synchronize()
+    assert torch.equal(y2, y2b)
+    idx2 = tile_sample_rows(5120, np.random.default_rng(4))
+    r2, b2 = oracle.q8_gemv(b, 5120, 17408, y1.cpu().numpy(), rows_idx=idx2)
+    assert_parity(y2.cpu().numpy()[:, idx2], r2, b2, "tc pdl chain")
+
+
+# ---------------------------------------------------------------------------
 # SSQ twin GEMV
 # ---------------------------------------------------------------------------
 def test_twin_256x512_seed0_matches_oracle():

@@ -1,8 +1,9 @@
 """A bounded pipeline wait that runs out, without faulting the GPU.
 
-The testing hook pti_test_q8_gemv_stall runs the fast-path Q8 GEMV with the
-first CTA's copy producer stopping before one unit (as if that copy never
-arrived) and every pipeline wait limited to 1 ms.  The consumer warps waiting
+The testing hook pti_test_q8_gemv_stall runs the fast-path Q8 GEMV (with
+either consumer: CUDA cores or tensor core) with the first CTA's copy
+producer stopping before one unit (as if that copy never arrived) and every
+pipeline wait limited to 1 ms.  The consumer warps waiting
 for the missing tile must give up, record PTI_DEVERR_FULL_TIMEOUT and wind
 down; every copy that was issued must have landed before the kernel exits (no
 PTI_DEVERR_DRAIN_TIMEOUT); the CUDA context, the stream and the library must
@@ -40,8 +41,9 @@ def first_cta_units(rows, cols):
     return units // min(sms, units, 320)
 
 
+@pytest.mark.parametrize("flags", [pti.FLAG_CUDA_CORES, pti.FLAG_TENSOR_CORES])
 @pytest.mark.parametrize("n", [1, 4])
-def test_stalled_copy_times_out_and_the_library_stays_usable(n):
+def test_stalled_copy_times_out_and_the_library_stays_usable(n, flags):
     rows, cols = 17408, 2048
     per_cta = first_cta_units(rows, cols)
     assert per_cta >= 7, "the shape must give the first CTA more units than the ring holds"
@@ -50,7 +52,7 @@ def test_stalled_copy_times_out_and_the_library_stays_usable(n):
     wd, xd = dev(w), dev(x)
     stream = torch.cuda.current_stream()
 
-    y_bad = pti.test_q8_gemv_stall(wd, rows, cols, xd, stall_unit=per_cta - 1, wait_ns=1_000_000)
+    y_bad = pti.test_q8_gemv_stall(wd, rows, cols, xd, stall_unit=per_cta - 1, wait_ns=1_000_000, flags=flags)
     torch.cuda.synchronize()                       # no CUDA error: the kernel returned
     err = pti.device_error()
     assert err & FULL_TIMEOUT, f"device error word {err:#x}: the consumers' wait did not run out"
@@ -59,7 +61,7 @@ def test_stalled_copy_times_out_and_the_library_stays_usable(n):
     del y_bad
 
     # the same stream, the same workspace: a normal call is exact again
-    y = pti.q8_gemv_nstream(wd, rows, cols, xd, stream=stream).cpu().numpy()
+    y = pti.q8_gemv_nstream(wd, rows, cols, xd, stream=stream, flags=flags).cpu().numpy()
     idx = np.unique(np.concatenate([np.arange(0, rows, 97), [rows - 1]])).astype(np.int64)
     y_ref, bound = oracle.q8_gemv(w, rows, cols, x, rows_idx=idx)
     assert np.all(np.abs(y[:, idx] - y_ref) <= 1e-5 * bound)
