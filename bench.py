@@ -49,7 +49,7 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-GEMV_SOURCES = ("pti_gemv_kernel.cuh", "pti_gemv.cu", "pti_device.cuh", "pti_host.h")
+GEMV_SOURCES = ("pti_gemv_kernel.cuh", "pti_gemv_tc.cuh", "pti_gemv.cu", "pti_device.cuh", "pti_host.h")
 DECODE_SOURCES = GEMV_SOURCES + ("pti_decode.cu",)
 VERIFY_SOURCES = ("pti_verify.cu", "pti_device.cuh", "pti_host.h")
 
@@ -182,7 +182,8 @@ class Q8Pass:
         self.pti, self.torch = pti, torch
         self.rows, self.cols, self.n, self.layers = rows, cols, n, layers
         self.flags = flags  # FLAG_TENSOR_CORES: the tensor-core consumer
-        self.name = f"q8_gemv_n{n}_{rows}x{cols}_x{layers}"
+        tc = bool(flags & pti.FLAG_TENSOR_CORES)
+        self.name = f"q8_gemv_n{n}_{rows}x{cols}_x{layers}" + ("_tensor_cores" if tc else "")
         self.w = w if w is not None else [pti_synth.q8_matrix_device(rows, cols, seed, 1000 + i)
                                           for i in range(layers)]
         self.x = pti_synth.activations_device(n, cols, seed, 1)
@@ -196,7 +197,7 @@ class Q8Pass:
         self.launches_per_step = 2 * layers
         self.gemv_launches_per_step = layers
         self.tokens_per_step = n
-        self.dominant = "gemv_tma_kernel<Q8,%d>" % n
+        self.dominant = ("gemv_tc_kernel<%d>" if tc else "gemv_tma_kernel<Q8,%d>") % n
         self.dtype = "f32"
         # FP32 FMA lane-operations: per weight N products and one dequantising FMA
         self.fma_ops_per_step = layers * rows * cols * (n + 1)
@@ -547,7 +548,8 @@ class SelfSpecLoop(Q8Pass):
 
 WORKLOADS = {
     "decode": lambda a: DecodePass(a.cols or 5120, a.rows or 17408, a.n, a.layers or 64),
-    "q8": lambda a: Q8Pass(a.rows or 17408, a.cols or 5120, a.n, a.layers or 16),
+    "q8": lambda a: Q8Pass(a.rows or 17408, a.cols or 5120, a.n, a.layers or 16,
+                           flags=0x4 if a.cores == "tensor" else 0),
     "twin": lambda a: TwinPass(a.rows or 17408, a.cols or 5120, a.layers or 8),
     "twin2": lambda a: TwinPass(a.rows or 17408, a.cols or 5120, a.layers or 8, per_model=2),
     "verify": lambda a: VerifyBatch(steps=a.vsteps),
@@ -718,6 +720,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0)
     ap.add_argument("--vsteps", type=int, default=4096, help="steps of the verify batches")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cores", default="cuda", choices=["cuda", "tensor"],
+                    help="q8 workload: the GEMV's products on the CUDA cores (default) or the tensor core")
     ap.add_argument("--no-q8-target", action="store_true",
                     help="decode line: skip the 17408x5120 Q8 GEMV timing at N = 1 and N = 4")
     a = ap.parse_args()
