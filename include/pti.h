@@ -108,9 +108,14 @@ const char *pti_status_string(pti_status status);
  * error (a different rounding order).  The fast path forms the products on
  * the CUDA cores (exact dequantisation, fp32 FMAs); with PTI_FLAG_TENSOR_CORES
  * (the _ex variant) on the tensor core instead (tcgen05.mma on binary16
- * operands that hold every weight and, split into three pieces, every fp32
- * activation exactly, with fp32 accumulation): same error bound, measured
- * no faster on GB300.
+ * operands that hold every weight exactly and every fp32 activation as three
+ * pieces, with fp32 accumulation), measured no faster on GB300.  That path's
+ * pieces are scaled per 32-column block and stream, and an activation 2^15
+ * or more below its block's largest loses bits: its error bound adds at most
+ * 2^-39 * sum_k |w_k| * (largest |x| in k's block) to the bar above (nothing
+ * for blocks whose values lie within a factor 2^15 of each other).  A
+ * non-finite activation gives non-finite outputs on both paths (NaN on the
+ * tensor core where the CUDA cores may give an infinity).
  */
 size_t pti_q8_gemv_workspace_bytes(int64_t rows, int64_t cols, int n_streams);
 
