@@ -681,13 +681,14 @@ def q8_target(a, world, local, peak, peak_kind):
     same harness (16 distinct matrices per step, launches after the first
     chained by programmatic dependent launch, CUDA-graph replay): time per
     GEMV, effective GB/s, fractions of the measured and the nominal HBM rate,
-    and the step-time ratio N=4 / N=1; also N=4 with the products on the
-    tensor core (the opt-in consumer) for comparison."""
+    and the step-time ratios N / N=1 (N = 2, 3, 4); also N=4 with the products
+    on the tensor core (the opt-in consumer) for comparison."""
     import torch
     import stream_quantized_gemv_gb300 as pti
     out = {"shape": "17408x5120", "matrices_per_step": 16, "steps": a.steps}
     shared = None
-    for n, key, flags in ((1, "n1", 0), (4, "n4", 0), (4, "n4_tensor_cores", pti.FLAG_TENSOR_CORES)):
+    for n, key, flags in ((1, "n1", 0), (2, "n2", 0), (3, "n3", 0), (4, "n4", 0),
+                          (4, "n4_tensor_cores", pti.FLAG_TENSOR_CORES)):
         wl = Q8Pass(17408, 5120, n, 16, w=shared, flags=flags)
         shared = wl.w
         ms, clocks = time_gpu(wl, a.steps, a.warmup, world, local)
@@ -698,6 +699,8 @@ def q8_target(a, world, local, peak, peak_kind):
                         "stream_tokens_per_s": round(n / (us * 1e-6), 1), "clocks": clocks}
         del wl
     out["ratio_n4_over_n1"] = round(out["n4"]["us_per_gemv"] / out["n1"]["us_per_gemv"], 4)
+    out["ratio_n2_over_n1"] = round(out["n2"]["us_per_gemv"] / out["n1"]["us_per_gemv"], 4)
+    out["ratio_n3_over_n1"] = round(out["n3"]["us_per_gemv"] / out["n1"]["us_per_gemv"], 4)
     out["peak_kind"] = peak_kind
     del shared
     torch.cuda.empty_cache()

@@ -49,11 +49,12 @@ def test_decode_line_carries_the_contract():
 
     # the 17408 x 5120 Q8 GEMV at one and four streams, same harness
     q = d["q8_target"]
-    for n in ("n1", "n4", "n4_tensor_cores"):
+    for n in ("n1", "n2", "n3", "n4", "n4_tensor_cores"):
         assert q[n]["us_per_gemv"] > 0 and q[n]["gbs"] > 0
         assert q[n]["of_measured"] == pytest.approx(q[n]["gbs"] / r["peak"], rel=2e-3)
         assert isinstance(q[n]["clocks"]["reasons"], list)
     assert q["ratio_n4_over_n1"] == pytest.approx(q["n4"]["us_per_gemv"] / q["n1"]["us_per_gemv"], rel=1e-3)
+    assert q["ratio_n2_over_n1"] == pytest.approx(q["n2"]["us_per_gemv"] / q["n1"]["us_per_gemv"], rel=1e-3)
 
     e = d["e2e"]
     assert e["value"] > 0 and e["unit"] == "GB/s"
