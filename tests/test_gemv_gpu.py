@@ -203,6 +203,17 @@ def test_tc_small_shapes_match_oracle(rows, cols, n):
     assert_parity(y, y_ref, bound, f"tc {rows}x{cols} n={n}")
 
 
+def test_cuda_core_flag_is_the_default_path():
+    """PTI_FLAG_CUDA_CORES selects the default consumer: bit-identical results."""
+    rows, cols = 1000, 2048
+    w = dev(pti_synth.q8_matrix(rows, cols, seed=13))
+    for n in (1, 4):
+        x = dev(pti_synth.activations(n, cols, seed=13, tensor_id=n))
+        a = pti.q8_gemv_nstream(w, rows, cols, x).clone()
+        b = pti.q8_gemv_nstream(w, rows, cols, x, flags=pti.FLAG_CUDA_CORES).clone()
+        assert torch.equal(a, b)
+
+
 def test_tc_exact_cases():
     """One-hot x, integer x with unit scales, extreme bytes: results exact in
     fp32 on the tensor core too (every product and partial sum is)."""
