@@ -238,3 +238,20 @@ def test_decode_pass_full_size_two_layers():
     check_layer(got2, xo, tol, "full size layer 2")
     del layers_dev, w
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("n", [1, 2, 3])
+def test_decode_pass_full_size_fewer_streams(n):
+    """hidden 5120, ffn 17408 with one to three streams: one layer, every
+    output checked (the four-stream case is the two-layer test above)."""
+    hidden, ffn = 5120, 17408
+    gd = pti_synth.q8_matrix_device(ffn, hidden, 7, 0)
+    ud = pti_synth.q8_matrix_device(ffn, hidden, 7, 1)
+    dd = pti_synth.q8_matrix_device(hidden, ffn, 7, 2)
+    x = pti_synth.activations(n, hidden, 7, 1000 + n)
+    got = run_pass(pti.DecodeWeights([gd], [ud], [dd]), 1, hidden, ffn, dev(x))
+    g, u, d = gd.cpu().numpy(), ud.cpu().numpy(), dd.cpu().numpy()
+    xo, tol = layer_tolerance(g, u, d, hidden, ffn, x)
+    check_layer(got, xo, tol, f"full size, {n} streams")
+    del gd, ud, dd
+    torch.cuda.empty_cache()
