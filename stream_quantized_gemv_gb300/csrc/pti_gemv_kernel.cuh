@@ -44,6 +44,9 @@
 //  * Programmatic dependent launch: the producer fetches its first weight
 //    tiles before waiting for the previous kernel in the stream, and only then
 //    fetches activations; nothing is written before that wait.
+//  * On request (PTI_FLAG_TENSOR_CORES) the Q8 kernel's products run on the
+//    tensor core instead: gemv_tc_kernel in pti_gemv_tc.cuh, the same ring,
+//    producer and tile finishing with a converter/MMA consumer side.
 //  * Epilogue modes (template parameter Epi) fuse the decode pass's glue into
 //    the tile epilogue: Plain writes y; GateUp reads 64 gate rows and the 64
 //    matching up rows into one tile and writes h = SiLU(b g) * (b u); Down

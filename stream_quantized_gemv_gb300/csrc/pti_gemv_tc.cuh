@@ -46,9 +46,10 @@
 // block w), warp 8 issues the copies (the CUDA-core kernel's producer), lane
 // 0 of warp 9 issues the MMAs and owns the tensor-memory allocation.
 //
-// Measured on GB300 (17408 x 5120, four streams, chained launches): 28.2 us
-// per GEMV against 28.4 us for the CUDA-core consumer, both bound by the
-// tensor core's instruction rate here rather than by HBM.  K = 16 per
+// Measured on GB300 (17408 x 5120, four streams, chained launches): about
+// 28.2 us per GEMV against 28.8 us for the CUDA-core consumer; this one is
+// bound by the tensor core's instruction rate, that one by its FMA pipe,
+// neither by HBM.  K = 16 per
 // kind::f16 instruction makes 16 MMAs per 128 x 256 unit; alone, one such MMA
 // (N <= 64) occupies the tensor pipe about 47 SM cycles whatever N, but with
 // the conversion's shared- and tensor-memory traffic running beside it, each
